@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Benchmark of the tiered-KV decode hot path on GB300.
+
+A step is one decode step of the whole attention stack over one batch: for
+every layer, append the new token's K/V, fetch that layer's T1 rows (and, on
+the first step after a re-tier, the delta of newly promoted rows) from pinned
+host memory, run decode attention over T0/T1/T2 with the fused attention-weight
+sums; then fold the scores; every Delta = 64 steps, re-tier.
+
+Default workload: the 7B-shaped attention stack (28 layers, 28/4 heads, d 128,
+batch 1) at the end of its 512 + 2000-token chain, T0 50 % / T1 47 % / T3 3 %.
+Inputs are synthetic (seeded generator), already in HBM for `value`; `e2e`
+repeats the timing with every step's q/k/v copied in from pinned host memory
+and the outputs copied back inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 7b|14b|32b|70b|tiny]
+                       [--impl tkv|reference]
+Under torchrun (N > 1) every rank runs its own replica (the path shards by
+sequence, with no data-path collective); the timing is max over ranks.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tiered decode-attn tokens/s (HBM GB/s vs peak); delta-prefetch PCIe GB/s"
+PRE_STEPS = 64            # decode steps before the first re-tier (scores accumulate)
+TARGET_N = {"tiny": 640, "7b": 2512, "14b": 4096, "32b": 8192, "70b": 16384}
+DESCR = {
+    "tiny": "Tiny: 1 layer, 4/2 heads, d 64, batch 1",
+    "7b": "7B-shaped attention stack: 28 layers, 28/4 heads, d 128, batch 1",
+    "14b": "14B-shaped: 48 layers, 40/8 heads, d 128, batch 8",
+    "32b": "32B-shaped: 64 layers, 40/8 heads, d 128, batch 4, T2 FP8-E4M3",
+    "70b": "70B-shaped: 80 layers, 64/8 heads, d 128, batch 8",
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=64)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["tkv", "reference"], default="tkv")
+    p.add_argument("--workload", default="7b", choices=sorted(TARGET_N))
+    p.add_argument("--t0", type=float, default=None, help="T0 (HBM) ratio; T1 takes the rest")
+    p.add_argument("--t3", type=float, default=None, help="eviction ratio")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--oracle-steps", type=int, default=0, help=argparse.SUPPRESS)
+    return p.parse_args()
+
+
+def bench_workload(name, warmup, steps, t0=None, t3=None):
+    from tiered_kv_cache_gqa_gb300 import synth
+    wl = synth.WORKLOADS[name]
+    r = list(wl.ratios)
+    if t3 is not None:
+        r[3] = t3
+    if t0 is not None:
+        r[0] = t0
+    if t0 is not None or t3 is not None:
+        r[1] = max(0.0, 1.0 - r[0] - r[2] - r[3])
+    n_pre = max(wl.prompt_len + wl.window + 1, TARGET_N[name] - PRE_STEPS - warmup - steps)
+    return wl.with_(ratios=tuple(r), prefill_len=n_pre, decode_steps=PRE_STEPS + warmup + steps)
+
+
+def describe(wl):
+    return ("%s; %d pre-filled positions (prompt %d) + %d decode steps (re-tier every %d); "
+            "tiers T0 %.0f%% T1 %.0f%% T2 %.0f%% T3 %.0f%%; sinks %d, window %d"
+            % (DESCR[wl.name], wl.prefill_len, wl.prompt_len, wl.decode_steps, wl.delta,
+               *(100 * x for x in wl.ratios), wl.num_sinks, wl.window))
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_run(wl, n_steps, seconds):
+    """Times the fp64 oracle's decode steps on this host (single-threaded BLAS).
+
+    Workloads too large for whole steps are sampled: one (sequence, layer) of a
+    step is timed and scaled by L * B.  Returns (tokens/s, description)."""
+    import numpy as np
+    from oracle import session
+    from tiered_kv_cache_gqa_gb300 import synth
+    gen = synth.Generator(wl, device="cpu")
+    full = wl.num_layers * wl.batch * wl.prefill_len <= 28 * 1 * 4096
+    if full:
+        sess = session.Session(wl.num_layers, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                               wl.batch, wl.prompt_len, wl.num_sinks, wl.window, wl.delta, wl.ratios)
+        K, V = gen.prefill()
+        sess.prefill(K.float().numpy(), V.float().numpy())
+        done, t_total = 0, 0.0
+        for t in range(1, 1 + max(1, n_steps or 10 ** 9)):
+            q, k, v = gen.decode_step(t)
+            a = (q.float().numpy(), k.float().numpy(), v.float().numpy())
+            t0 = time.perf_counter()
+            sess.step(*a)
+            t_total += time.perf_counter() - t0
+            done += 1
+            if not n_steps and t_total >= seconds:
+                break
+        return wl.batch * done / t_total, "%d full decode steps (all %d layers, batch %d)" % (
+            done, wl.num_layers, wl.batch)
+    # sampled: one sequence, one layer at a time, all positions of the workload
+    from oracle import attention
+    done, t_total = 0, 0.0
+    layer = 0
+    while True:
+        k, v = gen.kv_rows(0, layer, 0, wl.prefill_len)
+        Kl = k.transpose(0, 1).float().numpy()
+        Vl = v.transpose(0, 1).float().numpy()
+        q, _, _ = gen.decode_step(1) if done == 0 else (q, None, None)
+        t0 = time.perf_counter()
+        attention.attend(q[layer, 0].float().numpy().astype(np.float64), Kl, Vl, wl.group)
+        t_total += time.perf_counter() - t0
+        done += 1
+        layer = (layer + 1) % wl.num_layers
+        if (n_steps and done >= n_steps) or (not n_steps and t_total >= seconds):
+            break
+    per_step = t_total / done * wl.num_layers * wl.batch
+    return wl.batch / per_step, ("sampled: %d (sequence, layer) attention passes over %d positions, "
+                                 "scaled by L*B = %d" % (done, wl.prefill_len,
+                                                         wl.num_layers * wl.batch))
+
+
+def oracle_worker(args):
+    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3)
+    v, what = oracle_run(wl, args.oracle_steps, args.cpu_seconds)
+    print(json.dumps({"value": v, "sample": what}))
+
+
+def cpu_baseline(args, steps=0):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", "--workload", args.workload,
+           "--steps", str(args.steps), "--warmup", str(args.warmup),
+           "--cpu-seconds", str(args.cpu_seconds), "--oracle-steps", str(steps)]
+    if args.t0 is not None:
+        cmd += ["--t0", str(args.t0)]
+    if args.t3 is not None:
+        cmd += ["--t3", str(args.t3)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("oracle worker failed:\n" + r.stderr[-2000:])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": out["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": out["sample"]}
+
+
+# -------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        rows = [l.split(",") for l in open(self.path) if l.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, x in zip(names, r[5:9]):
+                if x.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank, world):
+    import numpy as np
+    import torch
+    import tiered_kv_cache_gqa_gb300 as tkv
+    from tiered_kv_cache_gqa_gb300 import synth
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    tkv.load()
+    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3)
+    wl = wl.with_(seed=wl.seed + 1000 * rank)
+    L, B, Hq, Hkv, d = wl.num_layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    stream = torch.cuda.current_stream()
+    ctx = tkv.TieredKV.for_workload(wl, device=dev)
+    gen = synth.Generator(wl, device="cuda")
+    for l in range(L):
+        K, V = gen.prefill_layer(l)
+        ctx.append(l, K, V, wl.prefill_len)
+        del K, V
+    n_steps = PRE_STEPS + args.warmup + args.steps
+    inputs = [gen.decode_step(t) for t in range(1, n_steps + 1)]
+    out = torch.empty(L, B, Hq, d, dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # > 129 MB L2
+
+    def step(t, q, k, v):
+        for l in range(L):
+            ctx.append(l, k[l], v[l], 1)
+            if l == 0:
+                ctx.prefetch(0)
+            if l + 1 < L:
+                ctx.prefetch(l + 1)
+            ctx.decode_step(l, q[l], out[l])
+        if t % wl.delta == 0:
+            ctx.retier()
+
+    t = 0
+    for _ in range(PRE_STEPS + args.warmup):
+        t += 1
+        step(t, *inputs[t - 1])
+    ctx.sync()
+    torch.cuda.synchronize()
+
+    # ---- timed: inputs resident in HBM, L2 flushed between steps
+    launches0 = ctx.stats()["kernel_launches"]
+    t_first = t + 1
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(dev) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ctx.profile_begin()
+    for i in range(args.steps):
+        t += 1
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step(t, *inputs[t - 1])
+        ev[i][1].record(stream)
+    prof = ctx.profile_end()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    launches = ctx.stats()["kernel_launches"] - launches0
+    st = ctx.stats()
+
+    # ---- e2e: the same steps fed from pinned host buffers, outputs copied back
+    e2e = None
+    if not args.no_e2e:
+        host_in = [(q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory())
+                   for (q, k, v) in inputs[t_first - 1: t_first - 1 + args.steps]]
+        dq, dk, dv = (torch.empty_like(x) for x in inputs[0])
+        host_out = torch.empty(L, B, Hq, d, dtype=torch.float32).pin_memory()
+        # replay the same decode positions on a fresh context so both loops see the same state
+        ctx.close()
+        ctx = tkv.TieredKV.for_workload(wl, device=dev)
+        for l in range(L):
+            K, V = gen.prefill_layer(l)
+            ctx.append(l, K, V, wl.prefill_len)
+            del K, V
+        t = 0
+        for _ in range(PRE_STEPS + args.warmup):
+            t += 1
+            step(t, *inputs[t - 1])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        e0.record(stream)
+        for i in range(args.steps):
+            t += 1
+            qh, kh, vh = host_in[i]
+            dq.copy_(qh, non_blocking=True)
+            dk.copy_(kh, non_blocking=True)
+            dv.copy_(vh, non_blocking=True)
+            step(t, dq, dk, dv)
+            host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        h2d = sum(x.numel() * x.element_size() for x in host_in[0])
+        d2h = host_out.numel() * host_out.element_size()
+        e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+    ctx.close()
+    return {"total_ms": total_ms, "step_ms": step_ms, "prof": prof, "stats": st, "clocks": clocks,
+            "launches": launches, "wl": wl, "e2e": e2e}
+
+
+def main():
+    args = parse()
+    if args.oracle_worker:
+        oracle_worker(args)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3)
+
+    if args.impl == "reference":
+        if rank == 0:
+            v, what = oracle_run(wl, args.warmup + args.steps, args.cpu_seconds)
+            cores = 1
+            line = {"metric": METRIC, "impl": "reference", "value": v, "unit": "tokens/s",
+                    "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": 1000.0 * wl.batch / v, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                    "config": {"workload": describe(wl), "global_batch": wl.batch,
+                               "seq_len": TARGET_N[args.workload], "parallelism": "replicas"},
+                    "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores,
+                                     "kind": "oracle", "sample": what},
+                    "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line))
+        return
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # before any CUDA work in this process
+        cpu = cpu_baseline(args)
+    r = run_gpu(args, rank, world)
+    total_ms = r["total_ms"]
+    e2e_ms = r["e2e"]["ms"] if r["e2e"] else None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms, e2e_ms or 0.0], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), (float(t[1]) if e2e_ms is not None else None)
+    if rank != 0:
+        return
+    wl = r["wl"]
+    K = args.steps
+    tokens = wl.batch * K * world
+    value = tokens / (total_ms / 1e3)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except Exception:
+        hbm_peak, peak_src = 6800.0, "fallback"
+    pa, p1, pd = r["prof"]["attn"], r["prof"]["t1"], r["prof"]["delta"]
+    achieved = pa["bytes"] / (pa["ms"] / 1e3) / 1e9 if pa["ms"] > 0 else 0.0
+    st = r["stats"]
+    t1_gbs = p1["bytes"] / (p1["ms"] / 1e3) / 1e9 if p1["ms"] > 0 else None
+    delta_gbs = pd["bytes"] / (pd["ms"] / 1e3) / 1e9 if pd["ms"] > 0 else None
+    link_ms = p1["ms"] + pd["ms"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe(wl), "global_batch": wl.batch * world,
+                   "seq_len": TARGET_N[args.workload], "parallelism": "replicas (sequence shards)",
+                   "l2": "flushed between timed steps (256 MB write); step working set %.0f MB"
+                         % (st["kv_bytes_full_cache"] / 2 ** 20)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "kernel": "tkv::attn_kernel", "peak_source": peak_src,
+                     "launches": pa["count"], "avg_launch_us": 1e3 * pa["ms"] / max(1, pa["count"]),
+                     "bytes_per_launch": pa["bytes"] / max(1, pa["count"])},
+        "cpu_baseline": cpu,
+        "e2e": ({"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                 "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"]}
+                if e2e_ms else None),
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "detail": {
+            "attention_step_ms": pa["ms"] / K,
+            "t1_stream": {"gbs": t1_gbs, "bytes_per_step": p1["bytes"] / K, "ms_per_step": p1["ms"] / K},
+            "delta_prefetch": {"gbs": delta_gbs, "bytes": pd["bytes"], "ms": pd["ms"]},
+            "link_peak_gbs_nominal_pcie5x16": 64.0,
+            "transfer_overhead_copy_share": link_ms / total_ms,
+            "hbm_saved_bytes": st["kv_bytes_full_cache"] - st["hbm_bytes_kv_resident"],
+            "hbm_kv_resident_bytes": st["hbm_bytes_kv_resident"],
+            "kv_full_cache_bytes": st["kv_bytes_full_cache"],
+            "tier_count": st["tier_count"],
+            "step_ms_median": statistics.median(r["step_ms"]),
+        },
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

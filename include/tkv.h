@@ -1,0 +1,242 @@
+/*
+ * tkv.h -- tiered KV-cache decode attention for one GB300 GPU (sm_103a).
+ *
+ * The method ("Not All Thoughts Need HBM: Semantics-Aware Memory Hierarchy
+ * for LLM Reasoning"; gist.science summary and fugumt.com abstract) keeps
+ * every token of a reasoning chain in one of four tiers:
+ *
+ *   T0  HBM, full precision (bf16)          -- protected tokens and the most
+ *                                              important reasoning tokens
+ *   T1  pinned host DDR, full precision     -- fetched back into HBM before
+ *                                              each attention step
+ *   T2  8-bit (FP8-E4M3, one fp32 scale per token, layer and KV head, for K
+ *       and for V), kept in HBM and dequantised inside the attention load
+ *   T3  evicted (dropped from every store)
+ *
+ * ranked by the cumulative attention score
+ *     s_i(t) = s_i(t-1) + (1/|L|) sum_l (1/H) sum_h alpha_{l,h}(t)[i]
+ * ("Importance scoring") and re-tiered every Delta decode steps ("System
+ * implementation", Delta = 64).  The prompt, the first `num_sinks` tokens and
+ * the last `recent_window` tokens are protected and always in T0
+ * ("Four-tier classification").
+ *
+ * Conventions for every call:
+ *   - Device pointers are caller-owned CUDA device memory (e.g. a torch
+ *     tensor's data_ptr()) and must stay valid until the work enqueued on the
+ *     context's compute stream has completed.  Host pointers are caller-owned
+ *     and are only read or written during the call.
+ *   - All GPU work is enqueued asynchronously on the context's streams; calls
+ *     return without waiting unless their comment says they synchronise.
+ *   - No call aborts or traps.  Argument errors return TKV_EINVAL and change
+ *     nothing.  The first CUDA error (or a device-side status word set by a
+ *     kernel) poisons the context: that call returns TKV_ECUDA / TKV_ETIMEOUT /
+ *     TKV_ECAPACITY and every later call except tkv_destroy, tkv_get_stats and
+ *     tkv_status_string returns TKV_ESTATE.
+ *   - One context is used from one host thread at a time.
+ *
+ * Shapes: L layers, B sequences, Hq query heads, Hkv KV heads, G = Hq / Hkv,
+ * d = head_dim (64 or 128).  Query head h reads KV head h / G (GQA).
+ * All sequences of a batch advance together: they hold the same number N of
+ * positions.
+ */
+#ifndef TKV_H
+#define TKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TKV_OK = 0,
+    TKV_EINVAL = 1,     /* bad argument or call out of order; nothing changed */
+    TKV_ENOMEM = 2,     /* device or pinned host allocation failed */
+    TKV_ECUDA = 3,      /* a CUDA runtime call failed; context poisoned */
+    TKV_ECAPACITY = 4,  /* a tier store or the position capacity is full */
+    TKV_ETIMEOUT = 5,   /* a bounded device-side wait ran out; context poisoned */
+    TKV_ESTATE = 6      /* context poisoned by an earlier error */
+} tkv_status;
+
+typedef struct tkv_ctx tkv_ctx;
+
+typedef struct {
+    int32_t num_layers;       /* L >= 1 */
+    int32_t num_q_heads;      /* Hq, a multiple of num_kv_heads, Hq / Hkv <= 8 */
+    int32_t num_kv_heads;     /* Hkv >= 1 */
+    int32_t head_dim;         /* d: 64 or 128 */
+    int32_t batch;            /* B >= 1 */
+    int32_t max_tokens;       /* capacity of positions per sequence, <= 65536 */
+    int32_t prompt_len;       /* protected prompt [0, prompt_len) */
+    int32_t num_sinks;        /* protected attention sinks [0, num_sinks) */
+    int32_t recent_window;    /* protected recent window [N - W, N) */
+    int32_t retier_interval;  /* Delta; informational for callers (tkv_retier is explicit) */
+    float ratio_t0;           /* tier shares of N; held internally as parts per million */
+    float ratio_t1;
+    float ratio_t2;
+    float ratio_t3;
+    int32_t t0_capacity;      /* HBM T0 slots per sequence; 0 = max_tokens */
+    int32_t t1_capacity;      /* pinned-host T1 slots per sequence (and HBM staging rows); 0 = max_tokens */
+    int32_t t2_capacity;      /* T2 slots per sequence; 0 = max_tokens if ratio_t2 > 0, else 0 */
+    int32_t device;           /* CUDA device ordinal */
+    void* compute_stream;     /* cudaStream_t for attention, append, fold, re-tier; NULL = create a
+                                 non-blocking one (then order the caller's work with tkv_sync);
+                                 cudaStreamLegacy / cudaStreamPerThread are accepted */
+    void* copy_stream;        /* cudaStream_t for T1 prefetch and delta prefetch; NULL = create one */
+} tkv_config;
+
+typedef struct {
+    int64_t num_tokens;            /* N: positions per sequence so far */
+    int64_t step;                  /* decode steps completed */
+    int64_t retiers;               /* re-tiers completed */
+    int64_t tier_count[4];         /* tokens per tier, summed over the batch */
+    int64_t t1_rows_streamed;      /* T1 slots copied per layer per sequence per step (high-water mark) */
+    int64_t last_promoted;         /* last re-tier: tokens moved into T0 from T1/T2 (summed over batch) */
+    int64_t last_demoted_t1;       /* last re-tier: tokens moved T0 -> T1 */
+    int64_t last_quantised;        /* last re-tier: tokens moved into T2 */
+    int64_t last_evicted;          /* last re-tier: tokens newly evicted */
+    int64_t last_t2_to_t1;         /* last re-tier: tokens moved T2 -> T1 */
+    int64_t h2d_bytes_t1_stream;   /* cumulative bytes of the per-layer T1 stream */
+    int64_t h2d_bytes_delta;       /* cumulative bytes of delta prefetch (promotions) */
+    int64_t d2h_bytes_writeback;   /* cumulative bytes written back to the host stores */
+    int64_t hbm_bytes_allocated;   /* device bytes held by the context */
+    int64_t host_bytes_allocated;  /* pinned host bytes held by the context */
+    int64_t hbm_bytes_kv_resident; /* KV bytes in HBM now: T0 rows + T2 rows + T1 staging */
+    int64_t kv_bytes_full_cache;   /* bf16 KV bytes of all N positions (no tiering) */
+    int64_t kernel_launches;       /* kernels this context has launched (all kinds) */
+    int32_t status;                /* tkv_status of the context */
+    int32_t attn_splits;           /* CTAs per (sequence, KV head) of the last attention launch */
+} tkv_stats;
+
+/* Creates a context: device pools for T0 (bf16), T2 (fp8 + scales) and the
+ * two-deep T1 staging ring, pinned mapped host stores for T1 and for the
+ * full-precision copy of T2 rows, page tables and the score vector s.
+ * Every position starts in T0.  Ownership of *out passes to the caller.
+ * Errors: TKV_EINVAL (shape/ratio checks), TKV_ENOMEM, TKV_ECUDA. */
+tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out);
+
+/* Frees everything the context holds (after synchronising its streams). */
+void tkv_destroy(tkv_ctx* ctx);
+
+/* Appends n_tokens new positions for one layer ("Four-tier classification":
+ * new tokens fall in the recent window, so they enter T0).
+ * k, v: device bf16 [B][n_tokens][Hkv][d].
+ * Protocol: a group of n tokens opens with layer 0 and every layer is
+ * appended in order 0..L-1.  With n_tokens == 1 the group is a decode step:
+ * tkv_decode_step(layer) follows tkv_append(layer), and the step closes after
+ * tkv_decode_step(L-1).  With n_tokens > 1 (prefill) the positions are
+ * committed when layer L-1 is appended; pre-filled positions start with
+ * s = 0 and are not scored.
+ * Errors: TKV_EINVAL (layer out of order, NULL pointers, n_tokens < 1),
+ * TKV_ECAPACITY (max_tokens or T0 capacity would be exceeded; nothing changes). */
+tkv_status tkv_append(tkv_ctx* ctx, int32_t layer, const void* k, const void* v,
+                      int32_t n_tokens);
+
+/* Enqueues, on the copy stream, the fetch of `layer`'s T1 rows (full
+ * precision, pinned host -> HBM staging slot layer % 2) and, on the first step
+ * after a re-tier, the delta prefetch of the rows newly promoted into T0 for
+ * that layer ("Zero-approximation-error offloading": T1 rows are fetched
+ * before each attention step; "System implementation": asynchronous delta
+ * prefetch of newly promoted tokens only).  Call it for layer l+1 before
+ * tkv_decode_step(l) so the copy overlaps layer l's attention; if it was not
+ * called, tkv_decode_step(layer) issues it itself.
+ * Errors: TKV_EINVAL (layer out of range, or called twice for one layer in
+ * one step). */
+tkv_status tkv_prefetch(tkv_ctx* ctx, int32_t layer);
+
+/* Decode attention of one layer for the open decode step, over all retained
+ * positions (T0, T1, T2; T3 excluded) in logical order, with the softmax
+ * scale 1/sqrt(d).  Also emits, per retained position, the sum over this
+ * layer's query heads of the attention weights, and on the last layer folds
+ * them into s ("Importance scoring").  The result does not depend on which of
+ * T0 / T1 a token sits in (Proposition 1): the work split and the order of
+ * every sum depend only on the retained set.
+ * q: device bf16 [B][Hq][d].  out: device fp32 [B][Hq][d].
+ * Errors: TKV_EINVAL (no open decode step, layer not yet appended, or out of
+ * order), TKV_ECUDA. */
+tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* out);
+
+/* Re-tiers every sequence by its current scores ("System implementation":
+ * every Delta = 64 decode steps; the caller calls it when step % Delta == 0,
+ * after tkv_decode_step(L-1)).  Ranking key: s descending, lower position
+ * first on exact ties.  Counts: n_k = floor(ratio_k * N) with ratios held in
+ * parts per million; T0's count includes the protected set; T3 is cumulative
+ * and never gives a token back; after evictions T0, then T2, take their
+ * targets from the ranked list and T1 takes the remainder (T1 shrinks first,
+ * then T2, if the protected set is too large).
+ * Rows leaving T0 are written back to the host store or quantised here; rows
+ * entering T0 are fetched by the next step's tkv_prefetch.  Synchronises the
+ * compute stream once (reads back the move counts).
+ * Errors: TKV_EINVAL (a decode step or prefill group is open),
+ * TKV_ECAPACITY (a tier store is full; context poisoned), TKV_ECUDA. */
+tkv_status tkv_retier(tkv_ctx* ctx);
+
+/* Copies s to the host: dst [B][N] fp32.  Synchronises. */
+tkv_status tkv_get_scores(tkv_ctx* ctx, float* dst_host);
+
+/* Replaces s from the host: src [B][N] fp32 (test hook: feed given scores to
+ * the re-tier).  Synchronises. */
+tkv_status tkv_set_scores(tkv_ctx* ctx, const float* src_host);
+
+/* Copies the tier of every position to the host: dst [B][N] uint8 (0..3).
+ * Synchronises. */
+tkv_status tkv_get_tiers(tkv_ctx* ctx, uint8_t* dst_host);
+
+/* Moves every position to the given tier (test hook, e.g. for Proposition 1:
+ * same T3 set, different T0/T1 splits): src [B][N] uint8.  Data moves exactly
+ * as in tkv_retier.  An evicted position cannot be given back a tier
+ * (TKV_EINVAL, nothing changes).  Synchronises. */
+tkv_status tkv_set_tiers(tkv_ctx* ctx, const uint8_t* src_host);
+
+/* Inspection hook: copies the stored K and V rows of one position of one
+ * layer and sequence, from wherever its tier keeps them, to the host, and
+ * returns its tier in *tier_out.
+ *   T0 / T1: dst_host receives bf16 [2][Hkv][d] (K rows, then V rows) from
+ *            the HBM T0 pool or the pinned host T1 store; scales untouched.
+ *   T2:      dst_host receives the E4M3 codes uint8 [2][Hkv][d] and
+ *            scales_host the fp32 scales [2][Hkv] from the HBM T2 pool.
+ *   T3:      nothing is copied.
+ * dst_host must hold 2*Hkv*d*2 bytes; scales_host 2*Hkv floats (may be NULL
+ * when the caller knows the position is not in T2).  Synchronises.
+ * Errors: TKV_EINVAL (indices out of range). */
+tkv_status tkv_get_row(tkv_ctx* ctx, int32_t layer, int32_t seq, int32_t pos, void* dst_host,
+                       float* scales_host, int32_t* tier_out);
+
+/* Time and bytes of one kind of work between tkv_profile_begin and _end. */
+typedef struct {
+    double ms;          /* summed CUDA-event time of the timed launches or copies */
+    int64_t count;      /* launches or copies timed */
+    double bytes;       /* algorithmic bytes they moved */
+} tkv_prof_entry;
+
+/* Kernel and copy timing.  tkv_profile_begin clears the counters and, until
+ * tkv_profile_end, brackets with CUDA events (at most 16384 of each kind):
+ *   attn   -- every attention launch, on the compute stream, right around the
+ *             kernel (after its wait for the T1 fetch).  Bytes per launch and
+ *             sequence: 4*Hkv*d per T0/T1 row, 2*Hkv*d + 8*Hkv per T2 row
+ *             (codes + two fp32 scales), plus q (bf16) and out (fp32);
+ *   t1     -- every per-layer T1 copy (pinned host -> HBM staging) on the
+ *             copy stream; bytes = rows copied * 4*Hkv*d;
+ *   delta  -- every delta-prefetch gather of promoted rows on the copy stream;
+ *             bytes = rows gathered * 4*Hkv*d.
+ * tkv_profile_end synchronises, stops recording and fills the entries (any
+ * pointer may be NULL). */
+tkv_status tkv_profile_begin(tkv_ctx* ctx);
+tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t1,
+                           tkv_prof_entry* delta);
+
+/* Waits for all enqueued work and reports any device-side status word. */
+tkv_status tkv_sync(tkv_ctx* ctx);
+
+/* Counters and sizes; valid on a poisoned context too. */
+tkv_status tkv_get_stats(tkv_ctx* ctx, tkv_stats* out);
+
+/* Static string for a status code. */
+const char* tkv_status_string(tkv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TKV_H */

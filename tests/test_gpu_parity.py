@@ -1,0 +1,231 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances: attention output max-abs 2e-3 (bf16 inputs, fp32 accumulate);
+s within 1e-4 relative (+1e-7 absolute floor for s near 0); tiers and every
+stored byte bit-exact; outputs bitwise identical across T0/T1 splits."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import tiered_kv_cache_gqa_gb300 as tkv
+from oracle import fp8, tiering
+from tiered_kv_cache_gqa_gb300 import synth
+
+from harness import ATOL_OUT, check_scores, f64, gpu_step, lockstep, make_session, prefill_both
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_workload_lockstep():
+    """The Tiny configuration: 1 layer, 4/2 heads, d 64, 512 positions, 128 decode steps with
+    re-tiers after steps 64 and 128 (steps 65..128 read T1 from the staging ring and skip T3)."""
+    wl = synth.WORKLOADS["tiny"]
+    ctx, sess, worst = lockstep(wl, wl.decode_steps)
+    st = ctx.stats()
+    assert st["retiers"] == 2
+    assert st["tier_count"][1] > 0 and st["tier_count"][3] == math.floor(0.03 * 640)
+    assert st["h2d_bytes_t1_stream"] > 0
+
+
+SHAPES = {
+    # name: (L, Hq, Hkv, d, B, prefill, steps, ratios, outliers)
+    "g4_d128_b2_t2": (2, 16, 4, 128, 2, 900, 70, (0.40, 0.35, 0.15, 0.10), 0.01),
+    "g5_d128": (1, 40, 8, 128, 1, 700, 66, (0.50, 0.47, 0.0, 0.03), 0.0),
+    "g7_d128": (2, 28, 4, 128, 1, 1100, 66, (0.30, 0.67, 0.0, 0.03), 0.0),
+    "g8_d128_long": (1, 64, 8, 128, 1, 2100, 65, (0.30, 0.60, 0.05, 0.05), 0.001),
+    "g1_d64": (1, 3, 3, 64, 3, 300, 66, (0.5, 0.3, 0.1, 0.1), 0.0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_shapes_lockstep(name):
+    L, Hq, Hkv, d, B, pre, steps, ratios, orate = SHAPES[name]
+    wl = synth.Workload(name, L, Hq, Hkv, d, B, prompt_len=32, prefill_len=pre, decode_steps=steps,
+                        window=32, ratios=ratios, outlier_rate=orate, seed=hash(name) % 1000)
+    ctx, sess, worst = lockstep(wl, steps)
+    tiers = ctx.tiers()
+    if ratios[2] > 0:
+        assert (tiers == 2).any()
+    assert (tiers == 1).any() and (tiers == 3).any()
+
+
+def _split_tiers(N, wl, evicted, t1_share, rng):
+    prot = tiering.protected_mask(N, wl.prompt_len, wl.num_sinks, wl.window)
+    t = np.zeros(N, dtype=np.uint8)
+    t[evicted] = 3
+    free = np.nonzero(~prot & (t != 3))[0]
+    t[rng.permutation(free)[: int(round(t1_share * len(free)))]] = 1
+    return t
+
+
+def test_proposition_1_bitwise_across_hbm_split():
+    """Same evicted set, T0 share 30 / 50 / 70 %: outputs and scores must be bit-identical."""
+    wl = synth.Workload("prop1", 2, 16, 4, 128, 2, prompt_len=16, prefill_len=1500, decode_steps=3,
+                        window=16, ratios=(0.3, 0.67, 0.0, 0.03), seed=11)
+    gen = synth.Generator(wl)
+    K, V = gen.prefill()
+    steps = [gen.decode_step(t) for t in range(1, 4)]
+    rng = np.random.default_rng(3)
+    N = wl.prefill_len
+    prot = tiering.protected_mask(N, wl.prompt_len, wl.num_sinks, wl.window)
+    evicted = [rng.choice(np.nonzero(~prot)[0], size=60, replace=False) for _ in range(wl.batch)]
+    results = []
+    for t0_share in (0.3, 0.5, 0.7):
+        ctx = tkv.TieredKV.for_workload(wl)
+        for l in range(wl.num_layers):
+            ctx.append(l, K[l].contiguous().cuda(), V[l].contiguous().cuda(), N)
+        tiers = np.stack([_split_tiers(N, wl, evicted[b], 1 - t0_share, np.random.default_rng(b))
+                          for b in range(wl.batch)])
+        ctx.set_tiers(tiers)
+        assert np.array_equal(ctx.tiers(), tiers)
+        out = torch.empty(len(steps), wl.num_layers, wl.batch, wl.num_q_heads, wl.head_dim,
+                          device="cuda")
+        for i, (q, k, v) in enumerate(steps):
+            gpu_step(ctx, q.cuda(), k.cuda(), v.cuda(), out[i])
+        results.append((out.cpu(), ctx.scores(), ctx.stats()))
+    for o, s, st in results[1:]:
+        assert torch.equal(o, results[0][0])
+        assert np.array_equal(s, results[0][1])
+    assert results[0][2]["tier_count"][1] > results[2][2]["tier_count"][1]
+    # and the common result is the oracle's
+    sess = make_session(wl)
+    sess.prefill(K.float().numpy(), V.float().numpy())
+    t = np.zeros((wl.batch, N), dtype=np.uint8)
+    for b in range(wl.batch):
+        t[b, evicted[b]] = 3
+    sess.apply_tiers(t)
+    for i, (q, k, v) in enumerate(steps):
+        ref = sess.step(q.float().numpy(), k.float().numpy(), v.float().numpy(), auto_retier=False)
+        assert np.abs(results[0][0][i].numpy() - ref).max() <= ATOL_OUT
+    check_scores(results[0][1], sess.scores())
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_retier_bit_exact_on_fed_scores(seed):
+    """Tiers from fed fp32 scores (random, and with many exact ties) equal the oracle's."""
+    rng = np.random.default_rng(seed)
+    wl = synth.Workload("fed", 1, 8, 2, 64, 4, prompt_len=20, prefill_len=3000, decode_steps=1,
+                        window=50, ratios=(0.25, 0.45, 0.2, 0.1), seed=seed)
+    gen = synth.Generator(wl)
+    ctx = tkv.TieredKV.for_workload(wl)
+    prefill_both(ctx, None, gen)
+    old = np.zeros((wl.batch, wl.prefill_len), dtype=np.uint8)
+    ppm = tuple(tiering.ratio_ppm(r) for r in wl.ratios)
+    for rnd in range(3):
+        s = rng.random((wl.batch, wl.prefill_len)).astype(np.float32)
+        s[1] = np.round(s[1] * 4) / 4                 # heavy ties
+        s[2] = 0.0                                    # all equal
+        s[3, ::7] = s[3, 1::7][: len(s[3, ::7])] if rnd else s[3, ::7]
+        ctx.set_scores(s)
+        ctx.retier()
+        got = ctx.tiers()
+        for b in range(wl.batch):
+            want = tiering.assign_tiers(s[b].astype(np.float64), old[b], wl.prefill_len, wl.prompt_len,
+                                        wl.num_sinks, wl.window, ppm)
+            assert np.array_equal(got[b], want), (rnd, b, np.argwhere(got[b] != want)[:10].tolist())
+        old = got
+
+
+def test_stored_rows_byte_exact_through_every_move():
+    """T1 writeback, E4M3 codes and scales, delta prefetch back into T0 (from T1 and from T2):
+    every stored byte equals the original bf16 row or the oracle's quantisation of it."""
+    wl = synth.Workload("rows", 2, 8, 2, 128, 2, prompt_len=8, prefill_len=400, decode_steps=2,
+                        window=8, ratios=(0.5, 0.3, 0.15, 0.05), outlier_rate=0.02, seed=5)
+    gen = synth.Generator(wl)
+    ctx = tkv.TieredKV.for_workload(wl)
+    K, V = prefill_both(ctx, None, gen)
+    Kb = K.view(torch.int16).numpy().view(np.uint16)      # [L][B][n][Hkv][d] bf16 bits
+    Vb = V.view(torch.int16).numpy().view(np.uint16)
+    rng = np.random.default_rng(0)
+    N = wl.prefill_len
+    tiers = np.zeros((wl.batch, N), dtype=np.uint8)
+    for b in range(wl.batch):
+        tiers[b, 8 + rng.permutation(N - 16)[:150]] = 1
+        idx2 = np.nonzero(tiers[b] == 0)[0]
+        idx2 = idx2[(idx2 >= 8) & (idx2 < N - 8)]
+        tiers[b, rng.permutation(idx2)[:60]] = 2
+    ctx.set_tiers(tiers)
+
+    def original(l, b, i):
+        return np.stack([Kb[l, b, i], Vb[l, b, i]])       # [2][Hkv][d]
+
+    for b in range(wl.batch):
+        for l in range(wl.num_layers):
+            for i in np.nonzero(tiers[b] == 1)[0][:40]:
+                t, data, _ = ctx.row(l, b, int(i))
+                assert t == 1 and np.array_equal(data, original(l, b, i))
+            for i in np.nonzero(tiers[b] == 2)[0][:40]:
+                t, codes, scales = ctx.row(l, b, int(i))
+                assert t == 2
+                orig = np.stack([K[l, b, i].float().numpy(), V[l, b, i].float().numpy()])
+                for kv in range(2):
+                    for h in range(wl.num_kv_heads):
+                        c_ref, s_ref = fp8.quantise_row(orig[kv, h])
+                        assert scales[kv, h] == s_ref
+                        assert np.array_equal(codes[kv, h], c_ref)
+    # promote everything back to T0: rows come back through the delta prefetch of the next step
+    back = np.zeros_like(tiers)
+    ctx.set_tiers(back)
+    q, k, v = gen.decode_step(1)
+    out = torch.empty(wl.num_layers, wl.batch, wl.num_q_heads, wl.head_dim, device="cuda")
+    gpu_step(ctx, q.cuda(), k.cuda(), v.cuda(), out)
+    for b in range(wl.batch):
+        for l in range(wl.num_layers):
+            for i in list(np.nonzero(tiers[b] == 1)[0][:30]) + list(np.nonzero(tiers[b] == 2)[0][:30]):
+                t, data, _ = ctx.row(l, b, int(i))
+                assert t == 0 and np.array_equal(data, original(l, b, i)), (l, b, i)
+    st = ctx.stats()
+    assert st["last_promoted"] == int((tiers != 0).sum())
+
+
+def test_first_token_attends_to_itself():
+    """N = 1: alpha = 1 and o = v (closed form); s of that token becomes 1."""
+    ctx = tkv.TieredKV(num_layers=2, num_q_heads=8, num_kv_heads=2, head_dim=128, batch=2,
+                       max_tokens=8, prompt_len=0, num_sinks=0, recent_window=0,
+                       ratios=(1.0, 0.0, 0.0, 0.0))
+    g = torch.Generator().manual_seed(0)
+    q = torch.randn(2, 2, 8, 128, generator=g).bfloat16().cuda()
+    k = torch.randn(2, 2, 2, 128, generator=g).bfloat16().cuda()
+    v = torch.randn(2, 2, 2, 128, generator=g).bfloat16().cuda()
+    out = torch.empty(2, 2, 8, 128, device="cuda")
+    gpu_step(ctx, q, k, v, out)
+    want = v.float().repeat_interleave(4, dim=2)
+    assert torch.equal(out, want)
+    assert np.array_equal(ctx.scores(), np.ones((2, 1), dtype=np.float32))
+
+
+def test_everything_protected_and_empty_tiers():
+    """Prompt covers every position: a re-tier keeps all in T0, T1 is empty, no copies run."""
+    wl = synth.Workload("prot", 1, 4, 2, 64, 1, prompt_len=200, prefill_len=150, decode_steps=64,
+                        window=64, ratios=(0.2, 0.5, 0.0, 0.3), seed=2)
+    ctx, sess, worst = lockstep(wl, 64)
+    assert (ctx.tiers() == 0).all()
+    assert ctx.stats()["h2d_bytes_t1_stream"] == 0
+
+
+def test_call_order_and_capacity_errors_leave_context_usable():
+    ctx = tkv.TieredKV(num_layers=2, num_q_heads=4, num_kv_heads=2, head_dim=64, batch=1,
+                       max_tokens=10, prompt_len=2, num_sinks=1, recent_window=2,
+                       ratios=(0.5, 0.5, 0.0, 0.0))
+    k = torch.zeros(1, 12, 2, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 4, 64, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(1, 4, 64, device="cuda")
+    lib = tkv.load()
+    assert tkv.tkv_append(ctx.ctx, 1, k, k, 1) == tkv.TKV_EINVAL          # layer 0 first
+    assert tkv.tkv_append(ctx.ctx, 0, k, k, 11) == tkv.TKV_ECAPACITY       # beyond max_tokens
+    assert tkv.tkv_decode_step(ctx.ctx, 0, q, out) == tkv.TKV_EINVAL       # nothing open
+    assert tkv.tkv_retier(ctx.ctx) == tkv.TKV_OK
+    ctx.append(0, k, k, 10)
+    assert tkv.tkv_retier(ctx.ctx) == tkv.TKV_EINVAL                       # prefill group open
+    ctx.append(1, k, k, 10)
+    assert tkv.tkv_append(ctx.ctx, 0, k, k, 1) == tkv.TKV_ECAPACITY        # full
+    assert ctx.stats()["status"] == tkv.TKV_OK
+    assert ctx.tiers().shape == (1, 10)
+    bad = np.zeros((1, 10), dtype=np.uint8)
+    bad[0, 5] = 3
+    ctx.set_tiers(bad)
+    bad[0, 5] = 0
+    assert tkv.tkv_set_tiers(ctx.ctx, bad) == tkv.TKV_EINVAL               # no coming back from T3
+    ctx.sync()

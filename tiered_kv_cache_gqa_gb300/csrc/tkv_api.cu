@@ -1,0 +1,771 @@
+// Host runtime behind the C ABI declared in include/tkv.h: context, device
+// pools, pinned host stores, page tables, the step protocol, the per-layer T1
+// prefetch pipeline (copy stream) and the re-tier driver.
+//
+// Method: "Not All Thoughts Need HBM: Semantics-Aware Memory Hierarchy for
+// LLM Reasoning" (gist.science summary; fugumt.com abstract).  The per-layer
+// T1 fetch before each attention step follows "Zero-approximation-error
+// offloading"; the re-tier every Delta steps and the delta prefetch of newly
+// promoted rows follow "System implementation"; the tier counts and the
+// protected set follow "Four-tier classification".
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/tkv.h"
+#include "tkv_internal.cuh"
+
+using namespace tkv;
+
+struct tkv_ctx {
+    tkv_config cfg{};
+    int L = 0, B = 0, Hq = 0, Hkv = 0, G = 0, d = 0, Nmax = 0, S0 = 0, S1 = 0, S2 = 0;
+    int64_t ppm[4] = {0, 0, 0, 0};
+    int device = 0;
+    cudaStream_t compute = nullptr, copy = nullptr;
+    bool own_compute = false, own_copy = false;
+
+    // device
+    __nv_bfloat16* k0v0 = nullptr;
+    __nv_bfloat16* stage = nullptr;
+    uint8_t* t2 = nullptr;
+    uint8_t *tier = nullptr, *new_tier = nullptr, *forced = nullptr;
+    int32_t *slot = nullptr, *new_slot = nullptr, *free_scratch = nullptr;
+    float* s = nullptr;
+    uint32_t* rl_loc = nullptr;
+    int32_t *rl_pos = nullptr, *rl_count = nullptr;
+    float* g = nullptr;
+    int32_t *t0_free = nullptr, *t0_top = nullptr;
+    int4 *moves_now = nullptr, *moves_delta = nullptr;
+    RetierOut* outp = nullptr;
+    RetierParams* params = nullptr;
+    int32_t* err = nullptr;
+
+    // pinned host
+    __nv_bfloat16 *h1 = nullptr, *h2m = nullptr;      // host pointers
+    __nv_bfloat16 *d_h1 = nullptr, *d_h2m = nullptr;  // device views
+    RetierOut* h_outp = nullptr;
+    RetierParams* h_params = nullptr;
+    int32_t* h_err = nullptr;
+
+    cudaEvent_t ev_t1[2] = {nullptr, nullptr}, ev_attn[2] = {nullptr, nullptr}, ev_retier = nullptr;
+
+    // host mirrors (identical to the device values after every call)
+    int N = 0;                         // committed positions
+    std::vector<int> count[4];         // tokens per tier, per sequence
+    std::vector<int> R;                // retained positions, per sequence
+    int hw1 = 0;                       // T1 slots streamed per layer
+    int64_t step = 0, retiers = 0;
+
+    // protocol state
+    int open_n = 0, appended = 0, decoded = 0;
+    std::vector<char> prefetched;
+    int delta_max = 0;                 // pending delta moves (max over sequences), 0 = none
+
+    int splits_max = 1;
+    int last_splits = 0;
+
+    // timing (tkv_profile_begin / tkv_profile_end): kinds 0 attention, 1 T1 copy, 2 delta
+    static constexpr int kProfPairs = 16384;
+    std::vector<cudaEvent_t> prof_ev[3];   // 2 per pair, created on first use
+    int prof_used[3] = {0, 0, 0};
+    double prof_bytes[3] = {0, 0, 0};
+    bool profiling = false;
+    int64_t launches = 0;
+    tkv_status status = TKV_OK;
+    tkv_stats st{};
+    size_t hbm_alloc = 0, host_alloc = 0;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+tkv_status fail(tkv_ctx* c, tkv_status s) {
+    if (c && c->status == TKV_OK) c->status = s;
+    return s;
+}
+
+#define CK(x)                                                      \
+    do {                                                           \
+        cudaError_t e_ = (x);                                      \
+        if (e_ != cudaSuccess) {                                   \
+            (void)cudaGetLastError();                              \
+            return fail(ctx, TKV_ECUDA);                           \
+        }                                                          \
+    } while (0)
+
+#define CHECK_CTX()                                        \
+    do {                                                   \
+        if (!ctx) return TKV_EINVAL;                       \
+        if (ctx->status != TKV_OK) return TKV_ESTATE;      \
+    } while (0)
+
+int64_t to_ppm(float r) { return (int64_t)std::llround((double)r * 1000000.0); }
+int64_t count_of(int64_t ppm, int64_t n) { return ppm * n / 1000000; }
+
+template <typename T>
+cudaError_t dalloc(tkv_ctx* c, T** p, size_t n) {
+    if (n == 0) {
+        *p = nullptr;
+        return cudaSuccess;
+    }
+    cudaError_t e = cudaMalloc((void**)p, n * sizeof(T));
+    if (e == cudaSuccess) c->hbm_alloc += n * sizeof(T);
+    return e;
+}
+
+template <typename T>
+cudaError_t halloc(tkv_ctx* c, T** p, size_t n) {
+    if (n == 0) {
+        *p = nullptr;
+        return cudaSuccess;
+    }
+    cudaError_t e = cudaHostAlloc((void**)p, n * sizeof(T), cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e == cudaSuccess) c->host_alloc += n * sizeof(T);
+    return e;
+}
+
+int protected_count(int N, int prompt, int sinks, int W) {
+    const int a = std::min(N, std::max(prompt, sinks));
+    const int w0 = std::max(0, N - W);
+    return a + (N - std::max(a, w0));
+}
+
+size_t row_bytes_bf16(const tkv_ctx* c) { return (size_t)2 * c->Hkv * c->d * 2; }   // K+V, one layer
+
+void free_all(tkv_ctx* c) {
+    cudaFree(c->k0v0); cudaFree(c->stage); cudaFree(c->t2);
+    cudaFree(c->tier); cudaFree(c->new_tier); cudaFree(c->forced);
+    cudaFree(c->slot); cudaFree(c->new_slot); cudaFree(c->free_scratch);
+    cudaFree(c->s); cudaFree(c->rl_loc); cudaFree(c->rl_pos); cudaFree(c->rl_count);
+    cudaFree(c->g); cudaFree(c->t0_free); cudaFree(c->t0_top);
+    cudaFree(c->moves_now); cudaFree(c->moves_delta); cudaFree(c->outp); cudaFree(c->params);
+    cudaFree(c->err);
+    cudaFreeHost(c->h1); cudaFreeHost(c->h2m); cudaFreeHost(c->h_outp); cudaFreeHost(c->h_params);
+    cudaFreeHost(c->h_err);
+    for (int i = 0; i < 2; ++i) {
+        if (c->ev_t1[i]) cudaEventDestroy(c->ev_t1[i]);
+        if (c->ev_attn[i]) cudaEventDestroy(c->ev_attn[i]);
+    }
+    if (c->ev_retier) cudaEventDestroy(c->ev_retier);
+    for (auto& v : c->prof_ev)
+        for (cudaEvent_t e : v) cudaEventDestroy(e);
+    if (c->own_compute && c->compute) cudaStreamDestroy(c->compute);
+    if (c->own_copy && c->copy) cudaStreamDestroy(c->copy);
+    (void)cudaGetLastError();
+}
+
+// Brackets of timed work: prof_open before, prof_close after (no-ops unless profiling).
+bool prof_open(tkv_ctx* c, int kind, cudaStream_t st) {
+    if (!c->profiling || c->prof_used[kind] >= tkv_ctx::kProfPairs) return false;
+    return cudaEventRecord(c->prof_ev[kind][2 * c->prof_used[kind]], st) == cudaSuccess;
+}
+void prof_close(tkv_ctx* c, int kind, cudaStream_t st, double bytes) {
+    cudaEventRecord(c->prof_ev[kind][2 * c->prof_used[kind] + 1], st);
+    c->prof_used[kind]++;
+    c->prof_bytes[kind] += bytes;
+}
+
+// Reads the device status word; returns it (0 if clear).
+tkv_status read_device_status(tkv_ctx* ctx) {
+    if (cudaMemcpy(ctx->h_err, ctx->err, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(ctx, TKV_ECUDA);
+    }
+    if (*ctx->h_err) return fail(ctx, (tkv_status)*ctx->h_err);
+    return TKV_OK;
+}
+
+// Enqueues the delta moves left by the last re-tier for layers [l0, l1).
+tkv_status enqueue_delta(tkv_ctx* ctx, int l0, int l1, cudaStream_t st) {
+    if (ctx->delta_max <= 0) return TKV_OK;
+    MoveArgs m{};
+    m.moves = ctx->moves_delta;
+    m.counts = &ctx->outp[0].n_delta;
+    m.count_stride = (int)(sizeof(RetierOut) / sizeof(int32_t));
+    m.k0v0 = ctx->k0v0; m.t2 = ctx->t2; m.h1 = ctx->d_h1; m.h2m = ctx->d_h2m;
+    m.layer_begin = l0; m.layer_end = l1;
+    m.L = ctx->L; m.B = ctx->B; m.Hkv = ctx->Hkv; m.d = ctx->d; m.Nmax = ctx->Nmax;
+    m.S0 = ctx->S0; m.S1 = ctx->S1; m.S2 = ctx->S2;
+    m.max_count = ctx->delta_max;
+    int64_t n = 0;
+    for (int b = 0; b < ctx->B; ++b) n += ctx->h_outp[b].n_delta;
+    const int64_t bytes = n * (int64_t)(l1 - l0) * (int64_t)row_bytes_bf16(ctx);
+    const bool timed = prof_open(ctx, 2, st);
+    CK(launch_moves(m, st));
+    if (timed) prof_close(ctx, 2, st, (double)bytes);
+    ctx->launches++;
+    ctx->st.h2d_bytes_delta += bytes;
+    return TKV_OK;
+}
+
+// Re-tier core shared by tkv_retier (ranked) and tkv_set_tiers (forced).
+tkv_status run_retier(tkv_ctx* ctx, bool forced) {
+    const int N = ctx->N, B = ctx->B;
+    // a delta left by an earlier re-tier that no decode step has consumed yet
+    if (ctx->delta_max > 0) {
+        tkv_status r = enqueue_delta(ctx, 0, ctx->L, ctx->compute);
+        if (r != TKV_OK) return r;
+        ctx->delta_max = 0;
+    }
+    const int P = protected_count(N, ctx->cfg.prompt_len, ctx->cfg.num_sinks, ctx->cfg.recent_window);
+    const int64_t n0 = std::max<int64_t>(P, count_of(ctx->ppm[0], N));
+    const int64_t n2 = count_of(ctx->ppm[2], N);
+    const int64_t n3 = count_of(ctx->ppm[3], N);
+    for (int b = 0; b < B; ++b) {
+        RetierParams& p = ctx->h_params[b];
+        std::memset(&p, 0, sizeof(p));
+        p.forced = forced ? 1 : 0;
+        const int64_t t3 = ctx->count[3][b];
+        const int64_t n_cand = N - P - t3;
+        const int64_t e = std::min(std::max<int64_t>(n3 - t3, 0), n_cand);
+        const int64_t m = n_cand - e;
+        const int64_t c0 = std::min(n0 - P, m);
+        const int64_t c2 = std::min(n2, m - c0);
+        p.c0 = (int)c0;
+        p.c2 = (int)c2;
+        p.c1 = (int)(m - c0 - c2);
+        p.n_cand = (int)n_cand;
+    }
+    CK(cudaMemcpyAsync(ctx->params, ctx->h_params, B * sizeof(RetierParams), cudaMemcpyHostToDevice,
+                       ctx->compute));
+    RetierArgs a{};
+    a.s = ctx->s; a.tier = ctx->tier; a.slot = ctx->slot; a.forced = ctx->forced;
+    a.params = ctx->params; a.new_tier = ctx->new_tier; a.new_slot = ctx->new_slot;
+    a.free_scratch = ctx->free_scratch; a.rl_loc = ctx->rl_loc; a.rl_pos = ctx->rl_pos;
+    a.rl_count = ctx->rl_count; a.t0_free = ctx->t0_free; a.t0_top = ctx->t0_top;
+    a.moves_now = ctx->moves_now; a.moves_delta = ctx->moves_delta; a.outp = ctx->outp;
+    a.B = B; a.N = N; a.Nmax = ctx->Nmax; a.S0 = ctx->S0; a.S1 = ctx->S1; a.S2 = ctx->S2;
+    a.prompt_len = ctx->cfg.prompt_len; a.num_sinks = ctx->cfg.num_sinks;
+    a.window = ctx->cfg.recent_window;
+    CK(launch_retier(a, ctx->compute));
+    ctx->launches++;
+    CK(cudaMemcpyAsync(ctx->h_outp, ctx->outp, B * sizeof(RetierOut), cudaMemcpyDeviceToHost,
+                       ctx->compute));
+    CK(cudaStreamSynchronize(ctx->compute));
+    tkv_status ds = read_device_status(ctx);
+    if (ds != TKV_OK) return ds;
+
+    int hw = 0, max_now = 0, max_delta = 0;
+    int64_t k[8] = {0};
+    for (int b = 0; b < B; ++b) {
+        const RetierOut& o = ctx->h_outp[b];
+        if (o.error) return fail(ctx, (tkv_status)o.error);
+        for (int t = 0; t < 4; ++t) ctx->count[t][b] = o.count[t];
+        ctx->R[b] = N - o.count[3];
+        hw = std::max(hw, o.hw1);
+        max_now = std::max(max_now, o.n_now);
+        max_delta = std::max(max_delta, o.n_delta);
+        for (int q = 0; q < 7; ++q) k[q] += o.kinds[q];
+    }
+    ctx->hw1 = hw;
+    // rows leaving T0 / entering T2 or T1 from the host side: now, all layers
+    MoveArgs m{};
+    m.moves = ctx->moves_now;
+    m.counts = &ctx->outp[0].n_now;
+    m.count_stride = (int)(sizeof(RetierOut) / sizeof(int32_t));
+    m.k0v0 = ctx->k0v0; m.t2 = ctx->t2; m.h1 = ctx->d_h1; m.h2m = ctx->d_h2m;
+    m.layer_begin = 0; m.layer_end = ctx->L;
+    m.L = ctx->L; m.B = B; m.Hkv = ctx->Hkv; m.d = ctx->d; m.Nmax = ctx->Nmax;
+    m.S0 = ctx->S0; m.S1 = ctx->S1; m.S2 = ctx->S2;
+    m.max_count = max_now;
+    CK(launch_moves(m, ctx->compute));
+    if (max_now > 0) ctx->launches++;
+    CK(cudaEventRecord(ctx->ev_retier, ctx->compute));
+    ctx->delta_max = max_delta;
+
+    const int64_t rb = (int64_t)row_bytes_bf16(ctx) * ctx->L;
+    ctx->st.last_promoted = k[MV_T1_T0] + k[MV_T2_T0];
+    ctx->st.last_demoted_t1 = k[MV_T0_T1];
+    ctx->st.last_quantised = k[MV_T0_T2] + k[MV_T1_T2];
+    ctx->st.last_evicted = k[0];
+    ctx->st.last_t2_to_t1 = k[MV_T2_T1];
+    ctx->st.d2h_bytes_writeback += (k[MV_T0_T1] + k[MV_T0_T2] + k[MV_T1_T2] + k[MV_T2_T1]) * rb;
+    ctx->retiers++;
+    return TKV_OK;
+}
+
+tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
+    const int slotr = layer & 1;
+    CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_attn[slotr], 0));
+    CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_retier, 0));
+    if (ctx->hw1 > 0) {
+        const size_t pitch = (size_t)ctx->S1 * ctx->d * sizeof(__nv_bfloat16);
+        const size_t layer_elems = (size_t)2 * ctx->B * ctx->Hkv * ctx->S1 * ctx->d;
+        const __nv_bfloat16* src = ctx->h1 + (size_t)layer * layer_elems;
+        __nv_bfloat16* dst = ctx->stage + (size_t)slotr * layer_elems;
+        const size_t width = (size_t)ctx->hw1 * ctx->d * sizeof(__nv_bfloat16);
+        const size_t height = (size_t)2 * ctx->B * ctx->Hkv;
+        const bool timed = prof_open(ctx, 1, ctx->copy);
+        CK(cudaMemcpy2DAsync(dst, pitch, src, pitch, width, height, cudaMemcpyHostToDevice, ctx->copy));
+        if (timed) prof_close(ctx, 1, ctx->copy, (double)(width * height));
+        ctx->st.h2d_bytes_t1_stream += (int64_t)(width * height);
+    }
+    if (ctx->delta_max > 0) {
+        tkv_status r = enqueue_delta(ctx, layer, layer + 1, ctx->copy);
+        if (r != TKV_OK) return r;
+    }
+    CK(cudaEventRecord(ctx->ev_t1[slotr], ctx->copy));
+    ctx->prefetched[layer] = 1;
+    return TKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tkv_status_string(tkv_status s) {
+    switch (s) {
+        case TKV_OK: return "ok";
+        case TKV_EINVAL: return "invalid argument or call order";
+        case TKV_ENOMEM: return "out of memory";
+        case TKV_ECUDA: return "CUDA error";
+        case TKV_ECAPACITY: return "tier store or position capacity exceeded";
+        case TKV_ETIMEOUT: return "bounded device wait timed out";
+        case TKV_ESTATE: return "context poisoned by an earlier error";
+    }
+    return "unknown status";
+}
+
+tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
+    if (!cfg || !out) return TKV_EINVAL;
+    *out = nullptr;
+    const tkv_config& c = *cfg;
+    if (c.num_layers < 1 || c.num_kv_heads < 1 || c.num_q_heads < 1 || c.batch < 1) return TKV_EINVAL;
+    if (c.num_q_heads % c.num_kv_heads) return TKV_EINVAL;
+    const int G = c.num_q_heads / c.num_kv_heads;
+    if (G > 8 || (c.head_dim != 64 && c.head_dim != 128)) return TKV_EINVAL;
+    if (c.max_tokens < 1 || c.max_tokens > 65536) return TKV_EINVAL;
+    if (c.prompt_len < 0 || c.num_sinks < 0 || c.recent_window < 0) return TKV_EINVAL;
+    if (c.t0_capacity < 0 || c.t1_capacity < 0 || c.t2_capacity < 0) return TKV_EINVAL;
+    const float r[4] = {c.ratio_t0, c.ratio_t1, c.ratio_t2, c.ratio_t3};
+    int64_t ppm[4], sum = 0;
+    for (int i = 0; i < 4; ++i) {
+        if (!(r[i] >= 0.f && r[i] <= 1.f)) return TKV_EINVAL;
+        ppm[i] = to_ppm(r[i]);
+        sum += ppm[i];
+    }
+    if (std::llabs(sum - 1000000) > 8) return TKV_EINVAL;
+
+    tkv_ctx* ctx = new (std::nothrow) tkv_ctx();
+    if (!ctx) return TKV_ENOMEM;
+    ctx->cfg = c;
+    ctx->L = c.num_layers; ctx->B = c.batch; ctx->Hq = c.num_q_heads; ctx->Hkv = c.num_kv_heads;
+    ctx->G = G; ctx->d = c.head_dim; ctx->Nmax = c.max_tokens;
+    ctx->S0 = c.t0_capacity ? c.t0_capacity : c.max_tokens;
+    ctx->S1 = c.t1_capacity ? c.t1_capacity : c.max_tokens;
+    ctx->S2 = c.t2_capacity ? c.t2_capacity : (ppm[2] > 0 ? c.max_tokens : 0);
+    for (int i = 0; i < 4; ++i) ctx->ppm[i] = ppm[i];
+    ctx->device = c.device;
+    DeviceGuard guard(c.device);
+
+    auto bail = [&](tkv_status s) {
+        free_all(ctx);
+        delete ctx;
+        return s;
+    };
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || c.device < 0 || c.device >= ndev) {
+        (void)cudaGetLastError();
+        return bail(TKV_ECUDA);
+    }
+    if (cudaSetDevice(c.device) != cudaSuccess) return bail(TKV_ECUDA);
+
+    if (c.compute_stream) ctx->compute = (cudaStream_t)c.compute_stream;
+    else {
+        if (cudaStreamCreateWithFlags(&ctx->compute, cudaStreamNonBlocking) != cudaSuccess) return bail(TKV_ECUDA);
+        ctx->own_compute = true;
+    }
+    if (c.copy_stream) ctx->copy = (cudaStream_t)c.copy_stream;
+    else {
+        if (cudaStreamCreateWithFlags(&ctx->copy, cudaStreamNonBlocking) != cudaSuccess) return bail(TKV_ECUDA);
+        ctx->own_copy = true;
+    }
+
+    const size_t L = ctx->L, B = ctx->B, Hkv = ctx->Hkv, d = ctx->d, Nmax = ctx->Nmax;
+    const size_t S0 = ctx->S0, S1 = ctx->S1, S2 = ctx->S2;
+    bool ok = true;
+    auto A = [&](cudaError_t e) {
+        if (e != cudaSuccess) ok = false;
+    };
+    A(dalloc(ctx, &ctx->k0v0, L * 2 * B * Hkv * S0 * d));
+    A(dalloc(ctx, &ctx->stage, 2 * 2 * B * Hkv * S1 * d));
+    A(dalloc(ctx, &ctx->t2, L * 2 * B * Hkv * S2 * (d + 16)));
+    A(dalloc(ctx, &ctx->tier, B * Nmax));
+    A(dalloc(ctx, &ctx->new_tier, B * Nmax));
+    A(dalloc(ctx, &ctx->forced, B * Nmax));
+    A(dalloc(ctx, &ctx->slot, B * Nmax));
+    A(dalloc(ctx, &ctx->new_slot, B * Nmax));
+    A(dalloc(ctx, &ctx->free_scratch, B * std::max(S0, std::max(S1, S2))));
+    A(dalloc(ctx, &ctx->s, B * Nmax));
+    A(dalloc(ctx, &ctx->rl_loc, B * Nmax));
+    A(dalloc(ctx, &ctx->rl_pos, B * Nmax));
+    A(dalloc(ctx, &ctx->rl_count, B));
+    A(dalloc(ctx, &ctx->g, L * B * Hkv * Nmax));
+    A(dalloc(ctx, &ctx->t0_free, B * S0));
+    A(dalloc(ctx, &ctx->t0_top, B));
+    A(dalloc(ctx, &ctx->moves_now, B * Nmax));
+    A(dalloc(ctx, &ctx->moves_delta, B * Nmax));
+    A(dalloc(ctx, &ctx->outp, B));
+    A(dalloc(ctx, &ctx->params, B));
+    A(dalloc(ctx, &ctx->err, 1));
+    if (!ok) {
+        (void)cudaGetLastError();
+        return bail(TKV_ENOMEM);
+    }
+    A(halloc(ctx, &ctx->h1, L * 2 * B * Hkv * S1 * d));
+    A(halloc(ctx, &ctx->h2m, L * 2 * B * Hkv * S2 * d));
+    A(halloc(ctx, &ctx->h_outp, B));
+    A(halloc(ctx, &ctx->h_params, B));
+    A(halloc(ctx, &ctx->h_err, 1));
+    if (!ok) {
+        (void)cudaGetLastError();
+        return bail(TKV_ENOMEM);
+    }
+    if (ctx->h1 && cudaHostGetDevicePointer((void**)&ctx->d_h1, ctx->h1, 0) != cudaSuccess) return bail(TKV_ECUDA);
+    if (ctx->h2m && cudaHostGetDevicePointer((void**)&ctx->d_h2m, ctx->h2m, 0) != cudaSuccess) return bail(TKV_ECUDA);
+    std::memset(ctx->h_outp, 0, B * sizeof(RetierOut));
+
+    // page tables: empty; T0 free stack holds every slot, lowest on top
+    std::vector<int32_t> fr(B * S0);
+    for (size_t b = 0; b < B; ++b)
+        for (size_t j = 0; j < S0; ++j) fr[b * S0 + j] = (int32_t)(S0 - 1 - j);
+    std::vector<int32_t> top(B, (int32_t)S0);
+    bool e = true;
+    auto E = [&](cudaError_t x) {
+        if (x != cudaSuccess) e = false;
+    };
+    E(cudaMemcpy(ctx->t0_free, fr.data(), fr.size() * 4, cudaMemcpyHostToDevice));
+    E(cudaMemcpy(ctx->t0_top, top.data(), B * 4, cudaMemcpyHostToDevice));
+    E(cudaMemset(ctx->rl_count, 0, B * 4));
+    E(cudaMemset(ctx->tier, 0, B * Nmax));
+    E(cudaMemset(ctx->s, 0, B * Nmax * 4));
+    E(cudaMemset(ctx->outp, 0, B * sizeof(RetierOut)));
+    E(cudaMemset(ctx->err, 0, 4));
+    for (int i = 0; i < 2; ++i) {
+        E(cudaEventCreateWithFlags(&ctx->ev_t1[i], cudaEventDisableTiming));
+        E(cudaEventCreateWithFlags(&ctx->ev_attn[i], cudaEventDisableTiming));
+    }
+    E(cudaEventCreateWithFlags(&ctx->ev_retier, cudaEventDisableTiming));
+    if (!e) {
+        (void)cudaGetLastError();
+        return bail(TKV_ECUDA);
+    }
+
+    // kernel set-up: the largest cluster size whose largest launch fits.  A
+    // launch with R retained rows uses S = clamp(ceil(R / 256), 1, Smax) CTAs
+    // per cluster and runs of ceil(R / S) rows rounded up to 32, so a run is at
+    // most max(256, ceil(Nmax / Smax)) rows.
+    ctx->splits_max = 0;
+    for (int S = kMaxSplits; S >= 1; S >>= 1) {
+        const int cap = std::max(256, (int)((Nmax + S - 1) / S));
+        const int chunk = (cap + kRows - 1) / kRows * kRows;
+        const size_t smem = attention_smem_bytes(G, ctx->d, chunk);
+        if (smem > 227 * 1024) continue;
+        if (attention_prepare(G, ctx->d, smem) != cudaSuccess) return bail(TKV_ECUDA);
+        if (attention_cluster_fits(G, ctx->d, smem, S)) {
+            ctx->splits_max = S;
+            break;
+        }
+    }
+    if (ctx->splits_max < 1) return bail(TKV_EINVAL);
+    if (retier_prepare(retier_smem_bytes(ctx->S0, ctx->S1, ctx->S2)) != cudaSuccess) return bail(TKV_ECUDA);
+
+    for (int t = 0; t < 4; ++t) ctx->count[t].assign(B, 0);
+    ctx->R.assign(B, 0);
+    ctx->prefetched.assign(L, 0);
+    *out = ctx;
+    return TKV_OK;
+}
+
+void tkv_destroy(tkv_ctx* ctx) {
+    if (!ctx) return;
+    DeviceGuard guard(ctx->device);
+    if (ctx->compute) cudaStreamSynchronize(ctx->compute);
+    if (ctx->copy) cudaStreamSynchronize(ctx->copy);
+    free_all(ctx);
+    delete ctx;
+}
+
+tkv_status tkv_append(tkv_ctx* ctx, int32_t layer, const void* k, const void* v, int32_t n_tokens) {
+    CHECK_CTX();
+    if (!k || !v || n_tokens < 1 || layer < 0 || layer >= ctx->L) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    const int B = ctx->B;
+    if (ctx->open_n == 0) {
+        if (layer != 0) return TKV_EINVAL;
+        if (ctx->N + n_tokens > ctx->Nmax) return TKV_ECAPACITY;
+        for (int b = 0; b < B; ++b)
+            if (ctx->count[0][b] + n_tokens > ctx->S0) return TKV_ECAPACITY;
+        CK(launch_open(ctx->t0_free, ctx->t0_top, ctx->tier, ctx->slot, ctx->s, ctx->rl_loc, ctx->rl_pos,
+                       ctx->rl_count, B, ctx->Nmax, ctx->S0, ctx->N, n_tokens, ctx->compute));
+        ctx->launches += 2;
+        for (int b = 0; b < B; ++b) {
+            ctx->count[0][b] += n_tokens;
+            ctx->R[b] += n_tokens;
+        }
+        ctx->open_n = n_tokens;
+        ctx->appended = 0;
+        ctx->decoded = 0;
+        std::fill(ctx->prefetched.begin(), ctx->prefetched.end(), 0);
+    } else {
+        if (n_tokens != ctx->open_n || layer != ctx->appended) return TKV_EINVAL;
+    }
+    CK(launch_append_rows((const __nv_bfloat16*)k, (const __nv_bfloat16*)v, ctx->k0v0, ctx->slot, layer,
+                          B, ctx->Hkv, ctx->d, ctx->Nmax, ctx->S0, ctx->N, n_tokens, ctx->compute));
+    ctx->launches++;
+    ctx->appended++;
+    if (ctx->open_n > 1 && ctx->appended == ctx->L) {
+        ctx->N += ctx->open_n;
+        ctx->open_n = 0;
+    }
+    return TKV_OK;
+}
+
+tkv_status tkv_prefetch(tkv_ctx* ctx, int32_t layer) {
+    CHECK_CTX();
+    if (layer < 0 || layer >= ctx->L) return TKV_EINVAL;
+    if (ctx->open_n != 1 || ctx->prefetched[layer]) return TKV_EINVAL;
+    // staging slot layer % 2 is still read by layer - 2's attention until it is issued
+    if (layer >= 2 && ctx->decoded < layer - 1) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    return issue_prefetch(ctx, layer);
+}
+
+tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* out) {
+    CHECK_CTX();
+    if (!q || !out || layer < 0 || layer >= ctx->L) return TKV_EINVAL;
+    if (ctx->open_n != 1 || layer != ctx->decoded || layer >= ctx->appended) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    if (!ctx->prefetched[layer]) {
+        tkv_status r = issue_prefetch(ctx, layer);
+        if (r != TKV_OK) return r;
+    }
+    const int slotr = layer & 1;
+    CK(cudaStreamWaitEvent(ctx->compute, ctx->ev_t1[slotr], 0));
+
+    int rmax = 0;
+    for (int b = 0; b < ctx->B; ++b) rmax = std::max(rmax, ctx->R[b]);
+    int S = std::min(ctx->splits_max, std::max(1, (rmax + 255) / 256));
+    int chunk = ((rmax + S - 1) / S + kRows - 1) / kRows * kRows;
+    AttnArgs a{};
+    a.q = (const __nv_bfloat16*)q;
+    a.out = out;
+    a.k0v0 = ctx->k0v0;
+    a.stage = ctx->stage + (size_t)slotr * 2 * ctx->B * ctx->Hkv * ctx->S1 * ctx->d;
+    a.t2 = ctx->t2;
+    a.rl_loc = ctx->rl_loc;
+    a.rl_count = ctx->rl_count;
+    a.g = ctx->g;
+    a.err = ctx->err;
+    a.layer = layer; a.L = ctx->L; a.B = ctx->B; a.Hq = ctx->Hq; a.Hkv = ctx->Hkv; a.d = ctx->d;
+    a.Nmax = ctx->Nmax; a.S0 = ctx->S0; a.S1 = ctx->S1; a.S2 = ctx->S2;
+    a.splits = S; a.chunk = chunk;
+    a.qscale = (float)(1.4426950408889634 / std::sqrt((double)ctx->d));
+    const bool timed = prof_open(ctx, 0, ctx->compute);
+    CK(launch_attention(a, ctx->compute));
+    ctx->launches++;
+    if (timed) {
+        double bytes = (double)ctx->B * ctx->Hq * ctx->d * (2 + 4);
+        for (int b = 0; b < ctx->B; ++b)
+            bytes += (double)(ctx->count[0][b] + ctx->count[1][b]) * 4.0 * ctx->Hkv * ctx->d +
+                     (double)ctx->count[2][b] * (2.0 * ctx->Hkv * ctx->d + 8.0 * ctx->Hkv);
+        prof_close(ctx, 0, ctx->compute, bytes);
+    }
+    CK(cudaEventRecord(ctx->ev_attn[slotr], ctx->compute));
+    ctx->last_splits = S;
+    ctx->decoded++;
+    if (ctx->decoded == ctx->L) {
+        const float inv = (float)(1.0 / ((double)ctx->L * (double)ctx->Hq));
+        CK(launch_fold(ctx->g, ctx->rl_pos, ctx->rl_count, ctx->s, ctx->L, ctx->B, ctx->Hkv, ctx->Nmax, rmax,
+                       inv, ctx->compute));
+        ctx->launches++;
+        ctx->N += 1;
+        ctx->open_n = 0;
+        ctx->step++;
+        ctx->delta_max = 0;   // this step's prefetches applied the delta for every layer
+    }
+    return TKV_OK;
+}
+
+tkv_status tkv_retier(tkv_ctx* ctx) {
+    CHECK_CTX();
+    if (ctx->open_n != 0) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    return run_retier(ctx, false);
+}
+
+tkv_status tkv_get_scores(tkv_ctx* ctx, float* dst) {
+    CHECK_CTX();
+    if (!dst) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    CK(cudaStreamSynchronize(ctx->copy));
+    CK(cudaStreamSynchronize(ctx->compute));
+    if (ctx->N > 0)
+        CK(cudaMemcpy2D(dst, ctx->N * sizeof(float), ctx->s, ctx->Nmax * sizeof(float), ctx->N * sizeof(float),
+                        ctx->B, cudaMemcpyDeviceToHost));
+    return read_device_status(ctx);
+}
+
+tkv_status tkv_set_scores(tkv_ctx* ctx, const float* src) {
+    CHECK_CTX();
+    if (!src || ctx->open_n != 0) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    CK(cudaStreamSynchronize(ctx->compute));
+    if (ctx->N > 0)
+        CK(cudaMemcpy2D(ctx->s, ctx->Nmax * sizeof(float), src, ctx->N * sizeof(float), ctx->N * sizeof(float),
+                        ctx->B, cudaMemcpyHostToDevice));
+    return TKV_OK;
+}
+
+tkv_status tkv_get_tiers(tkv_ctx* ctx, uint8_t* dst) {
+    CHECK_CTX();
+    if (!dst) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    CK(cudaStreamSynchronize(ctx->copy));
+    CK(cudaStreamSynchronize(ctx->compute));
+    if (ctx->N > 0)
+        CK(cudaMemcpy2D(dst, ctx->N, ctx->tier, ctx->Nmax, ctx->N, ctx->B, cudaMemcpyDeviceToHost));
+    return read_device_status(ctx);
+}
+
+tkv_status tkv_set_tiers(tkv_ctx* ctx, const uint8_t* src) {
+    CHECK_CTX();
+    if (!src || ctx->open_n != 0) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    const int N = ctx->N, B = ctx->B;
+    std::vector<uint8_t> cur((size_t)B * N);
+    tkv_status r = tkv_get_tiers(ctx, cur.data());
+    if (r != TKV_OK) return r;
+    for (size_t i = 0; i < cur.size(); ++i) {
+        if (src[i] > 3) return TKV_EINVAL;
+        if (cur[i] == 3 && src[i] != 3) return TKV_EINVAL;
+    }
+    if (N > 0)
+        CK(cudaMemcpy2D(ctx->forced, ctx->Nmax, src, N, N, B, cudaMemcpyHostToDevice));
+    return run_retier(ctx, true);
+}
+
+tkv_status tkv_get_row(tkv_ctx* ctx, int32_t layer, int32_t seq, int32_t pos, void* dst,
+                       float* scales, int32_t* tier_out) {
+    CHECK_CTX();
+    if (!dst || !tier_out || layer < 0 || layer >= ctx->L || seq < 0 || seq >= ctx->B || pos < 0 ||
+        pos >= ctx->N)
+        return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    CK(cudaStreamSynchronize(ctx->copy));
+    CK(cudaStreamSynchronize(ctx->compute));
+    uint8_t t = 0;
+    int32_t sl = 0;
+    const size_t p = (size_t)seq * ctx->Nmax + pos;
+    CK(cudaMemcpy(&t, ctx->tier + p, 1, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&sl, ctx->slot + p, 4, cudaMemcpyDeviceToHost));
+    *tier_out = t;
+    const int d = ctx->d;
+    for (int kv = 0; kv < 2; ++kv) {
+        for (int h = 0; h < ctx->Hkv; ++h) {
+            const size_t o = (size_t)kv * ctx->Hkv + h;
+            if (t == 0) {
+                CK(cudaMemcpy((uint16_t*)dst + o * d,
+                              ctx->k0v0 + row_index(layer, kv, seq, h, sl, ctx->B, ctx->Hkv, ctx->S0) * d,
+                              (size_t)d * 2, cudaMemcpyDeviceToHost));
+            } else if (t == 1) {
+                std::memcpy((uint16_t*)dst + o * d,
+                            ctx->h1 + row_index(layer, kv, seq, h, sl, ctx->B, ctx->Hkv, ctx->S1) * d,
+                            (size_t)d * 2);
+            } else if (t == 2) {
+                const uint8_t* rec = ctx->t2 + row_index(layer, kv, seq, h, sl, ctx->B, ctx->Hkv, ctx->S2) * (d + 16);
+                CK(cudaMemcpy((uint8_t*)dst + o * d, rec, (size_t)d, cudaMemcpyDeviceToHost));
+                if (scales) CK(cudaMemcpy(scales + o, rec + d, 4, cudaMemcpyDeviceToHost));
+            }
+        }
+    }
+    return read_device_status(ctx);
+}
+
+tkv_status tkv_profile_begin(tkv_ctx* ctx) {
+    CHECK_CTX();
+    DeviceGuard guard(ctx->device);
+    for (int k = 0; k < 3; ++k) {
+        if (ctx->prof_ev[k].empty()) {
+            ctx->prof_ev[k].resize(2 * tkv_ctx::kProfPairs, nullptr);
+            for (auto& e : ctx->prof_ev[k]) CK(cudaEventCreate(&e));
+        }
+        ctx->prof_used[k] = 0;
+        ctx->prof_bytes[k] = 0.0;
+    }
+    ctx->profiling = true;
+    return TKV_OK;
+}
+
+tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t1, tkv_prof_entry* delta) {
+    CHECK_CTX();
+    DeviceGuard guard(ctx->device);
+    ctx->profiling = false;
+    CK(cudaStreamSynchronize(ctx->copy));
+    CK(cudaStreamSynchronize(ctx->compute));
+    tkv_prof_entry* outs[3] = {attn, t1, delta};
+    for (int k = 0; k < 3; ++k) {
+        double ms = 0.0;
+        for (int i = 0; i < ctx->prof_used[k]; ++i) {
+            float t = 0.f;
+            CK(cudaEventElapsedTime(&t, ctx->prof_ev[k][2 * i], ctx->prof_ev[k][2 * i + 1]));
+            ms += t;
+        }
+        if (outs[k]) {
+            outs[k]->ms = ms;
+            outs[k]->count = ctx->prof_used[k];
+            outs[k]->bytes = ctx->prof_bytes[k];
+        }
+    }
+    return read_device_status(ctx);
+}
+
+tkv_status tkv_sync(tkv_ctx* ctx) {
+    CHECK_CTX();
+    DeviceGuard guard(ctx->device);
+    CK(cudaStreamSynchronize(ctx->copy));
+    CK(cudaStreamSynchronize(ctx->compute));
+    return read_device_status(ctx);
+}
+
+tkv_status tkv_get_stats(tkv_ctx* ctx, tkv_stats* out) {
+    if (!ctx || !out) return TKV_EINVAL;
+    tkv_stats s = ctx->st;
+    s.num_tokens = ctx->N;
+    s.step = ctx->step;
+    s.retiers = ctx->retiers;
+    for (int t = 0; t < 4; ++t) {
+        s.tier_count[t] = 0;
+        for (int b = 0; b < ctx->B; ++b) s.tier_count[t] += ctx->count[t][b];
+    }
+    s.t1_rows_streamed = ctx->hw1;
+    s.hbm_bytes_allocated = (int64_t)ctx->hbm_alloc;
+    s.host_bytes_allocated = (int64_t)ctx->host_alloc;
+    const int64_t rb = (int64_t)row_bytes_bf16(ctx) * ctx->L;
+    const int64_t r2 = (int64_t)2 * ctx->Hkv * (ctx->d + 16) * ctx->L;
+    s.hbm_bytes_kv_resident = s.tier_count[0] * rb + s.tier_count[2] * r2 +
+                              (int64_t)2 * ctx->B * ctx->hw1 * (int64_t)row_bytes_bf16(ctx);
+    s.kv_bytes_full_cache = (int64_t)ctx->N * ctx->B * rb;
+    s.kernel_launches = ctx->launches;
+    s.status = ctx->status;
+    s.attn_splits = ctx->last_splits;
+    *out = s;
+    return TKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,242 @@
+// Internal definitions shared by the tkv CUDA sources (not part of the C ABI).
+//
+// Device-memory layout (all row-major, innermost last):
+//   T0 pool      k0v0  [L][2][B][Hkv][S0][d]        bf16   (2 = K, V)
+//   T1 staging   stage [2][2][B][Hkv][S1][d]        bf16   (ring of 2 layers)
+//   T2 pool      t2    [L][2][B][Hkv][S2][d + 16]   bytes: d E4M3 codes, then the
+//                                                   fp32 scale and 12 bytes of padding
+//   host T1      h1    [L][2][B][Hkv][S1][d]        bf16, pinned + mapped
+//   host master  h2m   [L][2][B][Hkv][S2][d]        bf16, pinned + mapped: full-precision
+//                                                   copy of every T2 row
+//   page tables  tier [B][Nmax] u8, slot [B][Nmax] i32, s [B][Nmax] f32
+//   retained     rl_loc [B][Nmax] u32 = tier << 30 | slot, rl_pos [B][Nmax] i32,
+//                rl_count [B]  -- non-evicted positions in logical order
+//   alpha sums   g [L][B][Hkv][Nmax] f32 (per retained index, this step)
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace tkv {
+
+constexpr int kMaxSplits = 16;          // CTAs per (sequence, KV head) cluster
+constexpr int kRows = 32;               // rows per pipeline stage
+constexpr int kConsumerWarps = 4;
+constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz: bound of every device wait
+
+// Move kinds produced by a re-tier.
+enum MoveKind : int {
+    MV_T0_T1 = 1,   // write back a T0 row to the host T1 store      (at re-tier)
+    MV_T0_T2 = 2,   // quantise a T0 row into T2, keep bf16 on host   (at re-tier)
+    MV_T1_T2 = 3,   // quantise a host T1 row into T2, keep bf16      (at re-tier)
+    MV_T2_T1 = 4,   // host master row -> host T1 store               (at re-tier)
+    MV_T1_T0 = 5,   // host T1 row -> T0                              (delta prefetch)
+    MV_T2_T0 = 6,   // host master row -> T0                          (delta prefetch)
+};
+
+// Per-sequence counters written by the re-tier kernel and read back once.
+struct RetierOut {
+    int32_t n_now;        // moves applied at re-tier time
+    int32_t n_delta;      // moves left for the delta prefetch
+    int32_t hw1;          // highest referenced T1 slot + 1
+    int32_t count[4];     // tokens per tier after the re-tier
+    int32_t kinds[8];     // moves per kind
+    int32_t error;        // 0 or a tkv_status
+    int32_t pad[2];
+};
+
+// Per-sequence parameters of a re-tier (computed on the host).
+struct RetierParams {
+    int32_t forced;       // 1: take tiers from `forced_tiers`, 0: rank by s
+    int32_t c0, c1, c2;   // ranked mode: candidates that go to T0 / T1 / T2
+    int32_t n_cand;       // unprotected, not yet evicted positions
+    int32_t pad[3];
+};
+
+__host__ __device__ inline uint32_t make_loc(int tier, int slot) {
+    return ((uint32_t)tier << 30) | (uint32_t)slot;
+}
+__host__ __device__ inline int loc_tier(uint32_t loc) { return (int)(loc >> 30); }
+__host__ __device__ inline int loc_slot(uint32_t loc) { return (int)(loc & 0x3FFFFFFFu); }
+
+// Row index of (layer, kv, b, head, slot) in a [L][2][B][Hkv][S] store.
+__host__ __device__ inline size_t row_index(int layer, int kv, int b, int h, int slot, int B,
+                                            int Hkv, int S) {
+    return ((((size_t)layer * 2 + kv) * B + b) * Hkv + h) * (size_t)S + slot;
+}
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(
+                     bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, at most kWaitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// Address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// bf16 pair packed in a 32-bit word -> two floats (exact).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Two E4M3 codes (low byte first) -> two floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t w) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)w, __NV_E4M3);
+    return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+}  // namespace tkv
+
+// Launchers (defined in the .cu files, called by the host runtime).
+namespace tkv {
+
+struct AttnArgs {
+    const __nv_bfloat16* q;      // [B][Hq][d]
+    float* out;                  // [B][Hq][d]
+    const __nv_bfloat16* k0v0;   // T0 pool (all layers)
+    const __nv_bfloat16* stage;  // staging ring slot for this layer: [2][B][Hkv][S1][d]
+    const uint8_t* t2;           // T2 pool (all layers)
+    const uint32_t* rl_loc;      // [B][Nmax]
+    const int32_t* rl_count;     // [B]
+    float* g;                    // [L][B][Hkv][Nmax]
+    int32_t* err;
+    int layer, L, B, Hq, Hkv, d, Nmax, S0, S1, S2;
+    int splits, chunk;           // CTAs per (b, kv head) and retained rows per CTA
+    float qscale;                // log2(e) / sqrt(d)
+};
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
+size_t attention_smem_bytes(int G, int d, int chunk);
+cudaError_t attention_prepare(int G, int d, size_t smem);
+bool attention_cluster_fits(int G, int d, size_t smem, int splits);
+
+cudaError_t launch_fold(const float* g, const int32_t* rl_pos, const int32_t* rl_count, float* s,
+                        int L, int B, int Hkv, int Nmax, int rmax, float inv_lh, cudaStream_t st);
+
+cudaError_t launch_open(int32_t* t0_free, int32_t* t0_top, uint8_t* tier, int32_t* slot, float* s,
+                        uint32_t* rl_loc, int32_t* rl_pos, int32_t* rl_count, int B, int Nmax,
+                        int S0, int N, int n, cudaStream_t st);
+
+cudaError_t launch_append_rows(const __nv_bfloat16* k, const __nv_bfloat16* v,
+                               __nv_bfloat16* k0v0, const int32_t* slot, int layer, int B,
+                               int Hkv, int d, int Nmax, int S0, int N, int n, cudaStream_t st);
+
+struct RetierArgs {
+    const float* s;
+    uint8_t* tier;
+    int32_t* slot;
+    const uint8_t* forced;       // [B][Nmax] or null
+    const RetierParams* params;  // [B]
+    uint8_t* new_tier;           // scratch [B][Nmax]
+    int32_t* new_slot;           // scratch [B][Nmax]
+    int32_t* free_scratch;       // scratch [B][max(S0,S1,S2)]
+    uint32_t* rl_loc;
+    int32_t* rl_pos;
+    int32_t* rl_count;
+    int32_t* t0_free;            // [B][S0]
+    int32_t* t0_top;             // [B]
+    uint32_t* resv1;             // [B][S1 words]
+    uint32_t* resv2;             // [B][S2 words]
+    int4* moves_now;             // [B][Nmax]
+    int4* moves_delta;           // [B][Nmax]
+    RetierOut* outp;             // [B]
+    int B, N, Nmax, S0, S1, S2, prompt_len, num_sinks, window;
+};
+
+cudaError_t launch_retier(const RetierArgs& a, cudaStream_t st);
+size_t retier_smem_bytes(int S0, int S1, int S2);
+cudaError_t retier_prepare(size_t smem);
+
+struct MoveArgs {
+    const int4* moves;           // [B][Nmax]
+    const int32_t* counts;       // per b: number of entries (stride count_stride ints)
+    int count_stride;
+    __nv_bfloat16* k0v0;
+    uint8_t* t2;
+    __nv_bfloat16* h1;           // device view of the host T1 store
+    __nv_bfloat16* h2m;          // device view of the host master store
+    int layer_begin, layer_end;  // layers handled by this launch
+    int L, B, Hkv, d, Nmax, S0, S1, S2;
+    int max_count;
+};
+
+cudaError_t launch_moves(const MoveArgs& a, cudaStream_t st);
+
+}  // namespace tkv
