@@ -226,6 +226,34 @@ tkv_status tkv_profile_begin(tkv_ctx* ctx);
 tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t1,
                            tkv_prof_entry* delta);
 
+/* Allocation-free decode step for callers that cannot let a library allocate
+ * device memory: runtimes whose caching allocator owns the whole memory
+ * budget, and decode loops that cannot afford the device-wide stalls that
+ * cudaMalloc / cudaFree may cause.  The paper has no counterpart: this is a
+ * packaging of the same attention kernel and score fold as tkv_decode_step,
+ * over a dense cache in which every position is retained and resident.
+ *   q:   device bf16 [L][B][Hq][d]
+ *   kv:  device bf16 [L][2][B][Hkv][R][d]   (K rows, then V rows; positions
+ *        0..R-1 in logical order, the decoded token included)
+ *   out: device fp32 [L][B][Hq][d]
+ *   s:   device fp32 [B][R], read and updated in place: s += the step's mean
+ *        over layers and query heads of the attention weights
+ *   stream: cudaStream_t to enqueue on (NULL = the legacy default stream)
+ * Scratch lives in fixed file-scope device arrays, held by every GPU that
+ * loads the library until exit: L*B*Hkv*R <= 2,097,152, B*R <= 262,144,
+ * B <= 256; larger sizes return TKV_ECAPACITY before anything is enqueued.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  The first
+ * call on a device (with that device current) resolves the scratch addresses
+ * and should come before any stream capture.  All calls share the scratch and
+ * leave their contents in it, so calls that overlap on the GPU race.  The call
+ * enqueues work and returns without waiting.
+ * Errors: TKV_EINVAL (NULL pointers, shapes), TKV_ECAPACITY (beyond the
+ * limits above), TKV_ECUDA. */
+tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, float* out, float* s,
+                                    int32_t num_layers, int32_t batch, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t num_positions,
+                                    void* stream);
+
 /* Waits for all enqueued work and reports any device-side status word. */
 tkv_status tkv_sync(tkv_ctx* ctx);
 

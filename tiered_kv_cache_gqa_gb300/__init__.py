@@ -23,7 +23,7 @@ TKV_OK, TKV_EINVAL, TKV_ENOMEM, TKV_ECUDA, TKV_ECAPACITY, TKV_ETIMEOUT, TKV_ESTA
 EXPORTS = ("tkv_create", "tkv_destroy", "tkv_append", "tkv_prefetch", "tkv_decode_step",
            "tkv_retier", "tkv_get_scores", "tkv_set_scores", "tkv_get_tiers", "tkv_set_tiers",
            "tkv_get_row", "tkv_profile_begin", "tkv_profile_end", "tkv_sync", "tkv_get_stats",
-           "tkv_status_string")
+           "tkv_status_string", "tkv_decode_dense_noalloc")
 
 
 class TkvUnavailable(RuntimeError):
@@ -107,6 +107,7 @@ def load():
     lib.tkv_profile_begin.argtypes = [vp]
     lib.tkv_profile_end.argtypes = [vp, ctypes.POINTER(ProfEntry), ctypes.POINTER(ProfEntry),
                                     ctypes.POINTER(ProfEntry)]
+    lib.tkv_decode_dense_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.tkv_sync.argtypes = [vp]
     lib.tkv_get_stats.argtypes = [vp, ctypes.POINTER(Stats)]
     lib.tkv_status_string.argtypes = [st]
@@ -199,6 +200,16 @@ def tkv_profile_end(ctx):
     e = [ProfEntry(), ProfEntry(), ProfEntry()]
     rc = load().tkv_profile_end(ctx, ctypes.byref(e[0]), ctypes.byref(e[1]), ctypes.byref(e[2]))
     return rc, {"attn": e[0].as_dict(), "t1": e[1].as_dict(), "delta": e[2].as_dict()}
+
+
+def tkv_decode_dense_noalloc(q, kv, out, s, num_layers, batch, num_q_heads, num_kv_heads,
+                             head_dim, num_positions, stream=None):
+    """Allocation-free decode step over a dense cache (see include/tkv.h); returns the status."""
+    if stream is None:
+        stream = torch_stream_handle()
+    return load().tkv_decode_dense_noalloc(_ptr(q), _ptr(kv), _ptr(out), _ptr(s), int(num_layers),
+                                           int(batch), int(num_q_heads), int(num_kv_heads),
+                                           int(head_dim), int(num_positions), ctypes.c_void_p(stream))
 
 
 def tkv_sync(ctx):

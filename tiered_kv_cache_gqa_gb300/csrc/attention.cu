@@ -483,6 +483,21 @@ cudaError_t attention_prepare(int G, int d, size_t smem) {
     return cudaErrorInvalidValue;
 }
 
+template <int G, int D>
+static cudaError_t ensure_smem_gd(size_t smem) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_kernel<G, D>);
+    if (e != cudaSuccess) return e;
+    if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
+    return prepare_gd<G, D>(smem);
+}
+
+cudaError_t attention_ensure_smem(int G, int d, size_t smem) {
+    if (d == 128) { TKV_DISPATCH_G(128, ensure_smem_gd, smem) }
+    if (d == 64) { TKV_DISPATCH_G(64, ensure_smem_gd, smem) }
+    return cudaErrorInvalidValue;
+}
+
 bool attention_cluster_fits(int G, int d, size_t smem, int splits) {
     if (d == 128) { TKV_DISPATCH_G(128, cluster_fits_gd, smem, splits) }
     if (d == 64) { TKV_DISPATCH_G(64, cluster_fits_gd, smem, splits) }

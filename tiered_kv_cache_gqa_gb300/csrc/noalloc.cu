@@ -1,0 +1,148 @@
+// Allocation-free decode step: tkv_decode_dense_noalloc.
+//
+// Some callers cannot let a library call cudaMalloc: a serving runtime whose
+// caching allocator owns the whole device-memory budget (memory the library
+// takes behind its back is not in that budget and can make the runtime's own
+// allocations fail), and latency-critical decode loops, because cudaMalloc and
+// cudaFree can synchronise the device and stall every stream on it.  This
+// entry point serves them: it runs the same attention kernel and score fold
+// as the context path, but its scratch -- the per-layer sums of attention
+// weights, the retained-index table and the per-sequence counts -- lives in
+// file-scope __device__ arrays of fixed size that every GPU which loads the
+// library holds until the process exits.
+//
+// Set-up: the first call on a device (with that device current) resolves the
+// arrays' device addresses with cudaGetSymbolAddress and checks which cluster
+// size fits; that first call should therefore come before any stream capture.
+// Every call shares the arrays and leaves its contents in them; calls that
+// overlap on the GPU (for example on two streams) race on them.
+#include <mutex>
+
+#include "../../include/tkv.h"
+#include "tkv_internal.cuh"
+
+using namespace tkv;
+
+namespace {
+
+constexpr size_t kMaxAlphaFloats = size_t(1) << 21;   // L*B*Hkv*R  <= 2,097,152  (8 MiB)
+constexpr size_t kMaxTable = size_t(1) << 18;         // B*R        <= 262,144    (1 MiB)
+constexpr int kMaxBatch = 256;
+
+static __device__ __align__(256) float g_alpha_scratch[kMaxAlphaFloats];
+static __device__ __align__(256) uint32_t g_index_scratch[kMaxTable];
+static __device__ __align__(256) int32_t g_count_scratch[kMaxBatch];
+static __device__ __align__(256) int32_t g_status_scratch[1];
+
+struct DevScratch {
+    bool ready = false;
+    float* alpha = nullptr;
+    uint32_t* index = nullptr;
+    int32_t* count = nullptr;
+    int32_t* status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+DevScratch g_dev[kMaxDevices];
+
+// Retained index j of sequence b at [b * R + j] (all rows live in T0 slot j),
+// count R per sequence, status word cleared.
+__global__ void noalloc_fill_kernel(uint32_t* index, int32_t* count, int32_t* status, int B, int R) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < B * R) index[i] = make_loc(0, i % R);
+    if (i < B) count[i] = R;
+    if (i == 0) status[0] = 0;
+}
+
+tkv_status setup(int dev, DevScratch** out) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    DevScratch& s = g_dev[dev];
+    if (!s.ready) {
+        if (cudaGetSymbolAddress((void**)&s.alpha, g_alpha_scratch) != cudaSuccess ||
+            cudaGetSymbolAddress((void**)&s.index, g_index_scratch) != cudaSuccess ||
+            cudaGetSymbolAddress((void**)&s.count, g_count_scratch) != cudaSuccess ||
+            cudaGetSymbolAddress((void**)&s.status, g_status_scratch) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return TKV_ECUDA;
+        }
+        s.ready = true;
+    }
+    *out = &s;
+    return TKV_OK;
+}
+
+}  // namespace
+
+extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, float* out, float* s,
+                                               int32_t num_layers, int32_t batch, int32_t num_q_heads,
+                                               int32_t num_kv_heads, int32_t head_dim,
+                                               int32_t num_positions, void* stream) {
+    const int L = num_layers, B = batch, Hq = num_q_heads, Hkv = num_kv_heads, d = head_dim;
+    const int R = num_positions;
+    if (!q || !kv || !out || !s) return TKV_EINVAL;
+    if (L < 1 || B < 1 || Hkv < 1 || Hq < 1 || R < 1 || Hq % Hkv || Hq / Hkv > 8 || (d != 64 && d != 128))
+        return TKV_EINVAL;
+    // size limits of the fixed scratch
+    if (B > kMaxBatch || (size_t)B * R > kMaxTable ||
+        (size_t)L * B * Hkv * R > kMaxAlphaFloats)
+        return TKV_ECAPACITY;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return TKV_ECUDA;
+    }
+    DevScratch* sc = nullptr;
+    tkv_status st0 = setup(dev, &sc);
+    if (st0 != TKV_OK) return st0;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int G = Hq / Hkv;
+
+    // same work split as the context path: S = clamp(ceil(R / 256), 1, largest cluster that fits)
+    int S = std::min(kMaxSplits, std::max(1, (R + 255) / 256));
+    int chunk = 0;
+    size_t smem = 0;
+    for (; S >= 1; --S) {
+        chunk = ((R + S - 1) / S + kRows - 1) / kRows * kRows;
+        smem = attention_smem_bytes(G, d, chunk);
+        if (smem > 227 * 1024) return TKV_ECAPACITY;
+        if (attention_ensure_smem(G, d, smem) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return TKV_ECUDA;
+        }
+        if (attention_cluster_fits(G, d, smem, S)) break;
+    }
+    if (S < 1) return TKV_ECUDA;
+
+    noalloc_fill_kernel<<<(B * R + 255) / 256, 256, 0, st>>>(sc->index, sc->count, sc->status, B, R);
+    if (cudaGetLastError() != cudaSuccess) return TKV_ECUDA;
+    AttnArgs a{};
+    a.out = out;
+    a.k0v0 = (const __nv_bfloat16*)kv;
+    a.stage = nullptr;
+    a.t2 = nullptr;
+    a.rl_loc = sc->index;
+    a.rl_count = sc->count;
+    a.g = sc->alpha;
+    a.err = sc->status;
+    a.L = L; a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.d = d;
+    a.Nmax = R; a.S0 = R; a.S1 = 0; a.S2 = 0;
+    a.splits = S; a.chunk = chunk;
+    a.qscale = (float)(1.4426950408889634 / std::sqrt((double)d));
+    for (int l = 0; l < L; ++l) {
+        a.layer = l;
+        a.q = (const __nv_bfloat16*)q + (size_t)l * B * Hq * d;
+        a.out = out + (size_t)l * B * Hq * d;
+        if (launch_attention(a, st) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return TKV_ECUDA;
+        }
+    }
+    const float inv = (float)(1.0 / ((double)L * (double)Hq));
+    if (launch_fold(sc->alpha, (const int32_t*)sc->index, sc->count, s, L, B, Hkv, R, R, inv, st) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return TKV_ECUDA;
+    }
+    return TKV_OK;
+}

@@ -186,6 +186,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
 size_t attention_smem_bytes(int G, int d, int chunk);
 cudaError_t attention_prepare(int G, int d, size_t smem);
 bool attention_cluster_fits(int G, int d, size_t smem, int splits);
+cudaError_t attention_ensure_smem(int G, int d, size_t smem);   // raises the cap, never lowers it
 
 cudaError_t launch_fold(const float* g, const int32_t* rl_pos, const int32_t* rl_count, float* s,
                         int L, int B, int Hkv, int Nmax, int rmax, float inv_lh, cudaStream_t st);
