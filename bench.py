@@ -51,6 +51,10 @@ def parse():
     p.add_argument("--workload", default="7b", choices=sorted(TARGET_N))
     p.add_argument("--t0", type=float, default=None, help="T0 (HBM) ratio; T1 takes the rest")
     p.add_argument("--t3", type=float, default=None, help="eviction ratio")
+    p.add_argument("--layers", type=int, default=None,
+                   help="override the layer count (small captures for ncu; per-launch size unchanged)")
+    p.add_argument("--t1", choices=["ce", "sm", "split"], default="ce",
+                   help="T1 transport: copy engine, SM copy kernel, or both")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -59,9 +63,11 @@ def parse():
     return p.parse_args()
 
 
-def bench_workload(name, warmup, steps, t0=None, t3=None):
+def bench_workload(name, warmup, steps, t0=None, t3=None, layers=None):
     from tiered_kv_cache_gqa_gb300 import synth
     wl = synth.WORKLOADS[name]
+    if layers:
+        wl = wl.with_(num_layers=layers)
     r = list(wl.ratios)
     if t3 is not None:
         r[3] = t3
@@ -74,10 +80,16 @@ def bench_workload(name, warmup, steps, t0=None, t3=None):
 
 
 def describe(wl):
-    return ("%s; %d pre-filled positions (prompt %d) + %d decode steps (re-tier every %d); "
+    layers = "" if wl.num_layers == synth_layers(wl.name) else " [%d layers only]" % wl.num_layers
+    return ("%s%s; %d pre-filled positions (prompt %d) + %d decode steps (re-tier every %d); "
             "tiers T0 %.0f%% T1 %.0f%% T2 %.0f%% T3 %.0f%%; sinks %d, window %d"
-            % (DESCR[wl.name], wl.prefill_len, wl.prompt_len, wl.decode_steps, wl.delta,
+            % (DESCR[wl.name], layers, wl.prefill_len, wl.prompt_len, wl.decode_steps, wl.delta,
                *(100 * x for x in wl.ratios), wl.num_sinks, wl.window))
+
+
+def synth_layers(name):
+    from tiered_kv_cache_gqa_gb300 import synth
+    return synth.WORKLOADS[name].num_layers
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -131,7 +143,7 @@ def oracle_run(wl, n_steps, seconds):
 
 
 def oracle_worker(args):
-    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3)
+    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3, args.layers)
     v, what = oracle_run(wl, args.oracle_steps, args.cpu_seconds)
     print(json.dumps({"value": v, "sample": what}))
 
@@ -146,6 +158,8 @@ def cpu_baseline(args, steps=0):
         cmd += ["--t0", str(args.t0)]
     if args.t3 is not None:
         cmd += ["--t3", str(args.t3)]
+    if args.layers:
+        cmd += ["--layers", str(args.layers)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("oracle worker failed:\n" + r.stderr[-2000:])
@@ -208,11 +222,12 @@ def run_gpu(args, rank, world):
     dev = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev)
     tkv.load()
-    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3)
+    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3, args.layers)
     wl = wl.with_(seed=wl.seed + 1000 * rank)
     L, B, Hq, Hkv, d = wl.num_layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     stream = torch.cuda.current_stream()
-    ctx = tkv.TieredKV.for_workload(wl, device=dev)
+    t1_mode = {"ce": tkv.TKV_T1_COPY_ENGINE, "sm": tkv.TKV_T1_SM_COPY, "split": tkv.TKV_T1_SPLIT}[args.t1]
+    ctx = tkv.TieredKV.for_workload(wl, device=dev, t1_transport=t1_mode)
     gen = synth.Generator(wl, device="cuda")
     for l in range(L):
         K, V = gen.prefill_layer(l)
@@ -278,7 +293,7 @@ def run_gpu(args, rank, world):
         host_out = torch.empty(L, B, Hq, d, dtype=torch.float32).pin_memory()
         # replay the same decode positions on a fresh context so both loops see the same state
         ctx.close()
-        ctx = tkv.TieredKV.for_workload(wl, device=dev)
+        ctx = tkv.TieredKV.for_workload(wl, device=dev, t1_transport=t1_mode)
         for l in range(L):
             K, V = gen.prefill_layer(l)
             ctx.append(l, K, V, wl.prefill_len)
@@ -321,7 +336,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
-    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3)
+    wl = bench_workload(args.workload, args.warmup, args.steps, args.t0, args.t3, args.layers)
 
     if args.impl == "reference":
         if rank == 0:
@@ -377,6 +392,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": describe(wl), "global_batch": wl.batch * world,
                    "seq_len": TARGET_N[args.workload], "parallelism": "replicas (sequence shards)",
+                   "t1_transport": args.t1,
                    "l2": "flushed between timed steps (256 MB write); step working set %.0f MB"
                          % (st["kv_bytes_full_cache"] / 2 ** 20)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",

@@ -61,6 +61,16 @@ typedef enum {
 
 typedef struct tkv_ctx tkv_ctx;
 
+/* T1 transports (tkv_config.t1_transport): the same bytes land in the same
+ * staging rows either way, so results do not depend on the choice.
+ *   TKV_T1_COPY_ENGINE  one cudaMemcpy2DAsync per layer on the copy stream
+ *   TKV_T1_SM_COPY      a copy kernel on the copy stream whose threads load
+ *                       the pinned host rows directly (zero-copy) and store
+ *                       them to staging
+ *   TKV_T1_SPLIT        half the rows by the copy engine, half by the copy
+ *                       kernel on a second stream, concurrently */
+enum { TKV_T1_COPY_ENGINE = 0, TKV_T1_SM_COPY = 1, TKV_T1_SPLIT = 2 };
+
 typedef struct {
     int32_t num_layers;       /* L >= 1 */
     int32_t num_q_heads;      /* Hq, a multiple of num_kv_heads, Hq / Hkv <= 8 */
@@ -79,6 +89,8 @@ typedef struct {
     int32_t t0_capacity;      /* HBM T0 slots per sequence; 0 = max_tokens */
     int32_t t1_capacity;      /* pinned-host T1 slots per sequence (and HBM staging rows); 0 = max_tokens */
     int32_t t2_capacity;      /* T2 slots per sequence; 0 = max_tokens if ratio_t2 > 0, else 0 */
+    int32_t t1_transport;     /* how the per-layer T1 rows reach HBM staging: TKV_T1_COPY_ENGINE,
+                                 TKV_T1_SM_COPY or TKV_T1_SPLIT (see below) */
     int32_t device;           /* CUDA device ordinal */
     void* compute_stream;     /* cudaStream_t for attention, append, fold, re-tier; NULL = create a
                                  non-blocking one (then order the caller's work with tkv_sync);

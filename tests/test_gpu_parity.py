@@ -229,3 +229,29 @@ def test_call_order_and_capacity_errors_leave_context_usable():
     bad[0, 5] = 0
     assert tkv.tkv_set_tiers(ctx.ctx, bad) == tkv.TKV_EINVAL               # no coming back from T3
     ctx.sync()
+
+
+def test_t1_transports_are_bitwise_identical():
+    """Copy engine, SM copy kernel and the split of both put the same bytes in the same staging
+    rows: outputs and scores are bit-identical, and match the oracle."""
+    wl = synth.Workload("t1x", 3, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
+                        window=16, ratios=(0.3, 0.6, 0.05, 0.05), seed=8)
+    outs = []
+    for mode in (tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T1_SM_COPY, tkv.TKV_T1_SPLIT):
+        gen = synth.Generator(wl)
+        ctx = tkv.TieredKV.for_workload(wl, t1_transport=mode)
+        prefill_both(ctx, None, gen)
+        res = []
+        out = torch.empty(wl.num_layers, wl.batch, wl.num_q_heads, wl.head_dim, device="cuda")
+        for t in range(1, 71):
+            q, k, v = gen.decode_step(t)
+            gpu_step(ctx, q.cuda(), k.cuda(), v.cuda(), out)
+            if t % 64 == 0:
+                ctx.retier()
+            if t > 64:
+                res.append(out.cpu().clone())
+        outs.append((torch.stack(res), ctx.scores(), ctx.stats()["h2d_bytes_t1_stream"]))
+    assert outs[0][2] > 0
+    for o, s, _ in outs[1:]:
+        assert torch.equal(o, outs[0][0])
+        assert np.array_equal(s, outs[0][1])

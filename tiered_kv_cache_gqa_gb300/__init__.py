@@ -15,9 +15,11 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtkv.so")
+# TKV_LIBRARY may name another build of the same library (e.g. a tuning variant).
+LIB_PATH = os.environ.get("TKV_LIBRARY") or os.path.join(_HERE, "libtkv.so")
 
 TKV_OK, TKV_EINVAL, TKV_ENOMEM, TKV_ECUDA, TKV_ECAPACITY, TKV_ETIMEOUT, TKV_ESTATE = range(7)
+TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY, TKV_T1_SPLIT = range(3)
 
 # Every function the C ABI exports (include/tkv.h).
 EXPORTS = ("tkv_create", "tkv_destroy", "tkv_append", "tkv_prefetch", "tkv_decode_step",
@@ -46,7 +48,8 @@ class Config(ctypes.Structure):
         ("ratio_t0", ctypes.c_float), ("ratio_t1", ctypes.c_float),
         ("ratio_t2", ctypes.c_float), ("ratio_t3", ctypes.c_float),
         ("t0_capacity", ctypes.c_int32), ("t1_capacity", ctypes.c_int32),
-        ("t2_capacity", ctypes.c_int32), ("device", ctypes.c_int32),
+        ("t2_capacity", ctypes.c_int32), ("t1_transport", ctypes.c_int32),
+        ("device", ctypes.c_int32),
         ("compute_stream", ctypes.c_void_p), ("copy_stream", ctypes.c_void_p),
     ]
 
@@ -241,7 +244,7 @@ class TieredKV:
     def __init__(self, *, num_layers, num_q_heads, num_kv_heads, head_dim, batch, max_tokens,
                  prompt_len, num_sinks=4, recent_window=64, retier_interval=64,
                  ratios=(1.0, 0.0, 0.0, 0.0), t0_capacity=0, t1_capacity=0, t2_capacity=0,
-                 device=0, compute_stream=None, copy_stream=None):
+                 t1_transport=TKV_T1_COPY_ENGINE, device=0, compute_stream=None, copy_stream=None):
         cfg = Config()
         cfg.num_layers, cfg.num_q_heads, cfg.num_kv_heads = num_layers, num_q_heads, num_kv_heads
         cfg.head_dim, cfg.batch, cfg.max_tokens = head_dim, batch, max_tokens
@@ -249,6 +252,7 @@ class TieredKV:
         cfg.retier_interval = retier_interval
         cfg.ratio_t0, cfg.ratio_t1, cfg.ratio_t2, cfg.ratio_t3 = ratios
         cfg.t0_capacity, cfg.t1_capacity, cfg.t2_capacity = t0_capacity, t1_capacity, t2_capacity
+        cfg.t1_transport = t1_transport
         cfg.device = device
         if compute_stream is None:
             compute_stream = torch_stream_handle()

@@ -14,72 +14,90 @@
 // tier a row sits in, and every sum below has a fixed order, so a row read
 // from T0 or from the T1 staging ring gives bit-identical results.
 //
-// Per CTA: warp 4 is the producer; it walks the run in tiles of 32 rows and,
-// per row, issues one 1-D bulk copy (cp.async.bulk) from the row's home --
-// T0 pool, T1 staging or T2 pool -- into a shared-memory ring whose stages
-// complete on mbarriers.  It streams the K rows of the whole run, then the V
-// rows.  Warps 0-3 consume:
+// Per CTA, four warps.  A warp owns the tiles w, w+4, ... (32 rows each) of the
+// CTA's run; it streams the K rows of its tiles, then their V rows, through its
+// own two-stage shared-memory ring with cp.async (16 bytes per lane, 16 lanes
+// per 256-byte row, each row fetched from its home: T0 pool, T1 staging or T2
+// pool), so loads for the next tile are in flight while the current one is
+// computed.  The only waits are cp.async.wait_group and hardware barriers.
 //   pass 1 (K): lane = row; z[h] = q'_h . k for the G query heads of the
-//              group, with q' = q * log2(e)/sqrt(d) held in shared memory
+//              group, with q' = q * log2(e)/sqrt(d) in shared memory
 //              (broadcast reads) and packed f32x2 FMAs; z is kept in shared
 //              memory; T2 rows: z = scale * (q' . code values).
 //   softmax:   per-CTA max m_h over the run, p = 2^(z - m_h) in place,
 //              l_h = sum p (fixed-order reduction).
-//   pass 2 (V): the warp walks a tile's rows; lane = 4 (or 2) columns;
+//   pass 2 (V): the warp walks its tiles' rows; lane = 4 (or 2) columns;
 //              O_h += p * v.
-// Cluster merge (distributed shared memory): every CTA reads all peers'
-// (m, l) in rank order -> M_h, L_h, per-peer factors f_r = 2^(m_r - M)/L; it
-// writes, for its own rows, g[j] = sum_h p_h[j] * f_self,h (the sum over the
-// group's query heads of alpha), and reduces its share of O over the peers in
-// rank order.  No atomics touch `out` or `g`.
+// Cluster merge (distributed shared memory): every CTA gathers all peers'
+// (m, l) -> M_h, L_h, per-peer factors f_r = 2^(m_r - M)/L; it writes, for its
+// own rows, g[j] = sum_h p_h[j] * f_self,h (the sum over the group's query
+// heads of alpha), and reduces its share of O over the peers in rank order.
+// No atomics touch `out` or `g`.
+#include <cmath>
+
 #include "tkv_internal.cuh"
 
 namespace tkv {
+
+#ifndef TKV_ATTN_WARPS
+#define TKV_ATTN_WARPS 4
+#endif
+#ifndef TKV_WARP_STAGES
+#define TKV_WARP_STAGES 2
+#endif
+constexpr int kAttnWarps = TKV_ATTN_WARPS;     // warps per CTA
+constexpr int kWarpStages = TKV_WARP_STAGES;   // ring stages per warp
 
 template <int G, int D>
 struct AttnCfg {
     static constexpr int GP = (G <= 4) ? 4 : 8;      // z / p row stride (floats)
     static constexpr int ROWB = 2 * D + 16;          // ring row stride (bytes), bank-skewed
-    static constexpr int NST = 6;                    // ring stages
     static constexpr int CPL = D / 32;               // pass-2 columns per lane
     static_assert(D == 64 || D == 128, "head_dim must be 64 or 128");
     static_assert(G >= 1 && G <= 8, "group size must be 1..8");
 
+    static constexpr size_t sz_stage = (size_t)kRows * ROWB;
+    static constexpr size_t sz_warp_ring = kWarpStages * sz_stage;
     static constexpr size_t off_ring = 0;
-    static constexpr size_t sz_ring = (size_t)NST * kRows * ROWB;
-    static constexpr size_t off_info = sz_ring;
-    static constexpr size_t off_bars = off_info + 16 * NST;
-    static constexpr size_t off_q = off_bars + 16 * NST;
-    static constexpr size_t off_o = off_q + (size_t)G * D * 4;
-    static constexpr size_t off_m = off_o + (size_t)G * D * 4;
+    static constexpr size_t off_q = kAttnWarps * sz_warp_ring;
+    static constexpr size_t off_o = off_q;   // O is written after q's last use
+    static constexpr size_t off_m = off_q + (size_t)G * D * 4;
     static constexpr size_t off_l = off_m + 32;
     static constexpr size_t off_f = off_l + 32;
-    static constexpr size_t off_red = off_f + (size_t)kMaxSplits * 8 * 4;
-    static constexpr size_t off_wm = off_red + 128 * 4;
-    static constexpr size_t off_flag = off_wm + kConsumerWarps * 8 * 4;
-    static constexpr size_t off_zp = off_flag + 16;
-    static_assert((size_t)kConsumerWarps * G * D * 4 <= sz_ring, "warp partials reuse the ring");
+    static constexpr size_t off_mall = off_f + (size_t)kMaxSplits * 8 * 4;
+    static constexpr size_t off_lall = off_mall + (size_t)kMaxSplits * 8 * 4;
+    static constexpr size_t off_red = off_lall + (size_t)kMaxSplits * 8 * 4;
+    static constexpr size_t off_wm = off_red + kAttnWarps * 32 * 4;
+    static constexpr size_t off_zp = off_wm + kAttnWarps * 8 * 4;
+    static_assert((size_t)G * D * 4 <= sz_warp_ring, "a warp's partial O reuses its ring");
 
-    // the CTA's slice of the retained list follows zp: chunk u32
+    // then z/p (chunk x GP floats) and the CTA's slice of the retained list (chunk u32)
     static size_t smem(int chunk) { return off_zp + (size_t)chunk * GP * 4 + (size_t)chunk * 4; }
 };
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kWarpStages - 1) : "memory");
+}
+
 template <int G, int D>
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
-    constexpr int GP = C::GP, ROWB = C::ROWB, NST = C::NST, CPL = C::CPL;
+    constexpr int GP = C::GP, ROWB = C::ROWB, CPL = C::CPL;
+    constexpr int NT = kAttnWarps * 32;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* ring = smem + C::off_ring;
-    uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::off_info);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::off_bars);
     float* q_s = reinterpret_cast<float*>(smem + C::off_q);
     float* o_s = reinterpret_cast<float*>(smem + C::off_o);
     float* m_s = reinterpret_cast<float*>(smem + C::off_m);
     float* l_s = reinterpret_cast<float*>(smem + C::off_l);
     float* f_s = reinterpret_cast<float*>(smem + C::off_f);
+    float* mall = reinterpret_cast<float*>(smem + C::off_mall);
+    float* lall = reinterpret_cast<float*>(smem + C::off_lall);
     float* red = reinterpret_cast<float*>(smem + C::off_red);
     float* wm = reinterpret_cast<float*>(smem + C::off_wm);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::off_flag);
     float* zp = reinterpret_cast<float*>(smem + C::off_zp);
     uint32_t* rl_s = reinterpret_cast<uint32_t*>(smem + C::off_zp + (size_t)a.chunk * GP * 4);
 
@@ -91,280 +109,253 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     const int j0 = rank * a.chunk;
     const int n = max(0, min(R, j0 + a.chunk) - j0);
     const int nst = (n + kRows - 1) / kRows;
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NST);
+    uint8_t* ring = smem + C::off_ring + (size_t)warp * C::sz_warp_ring;
 
-    if (tid == 0) {
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    for (int i = tid; i < G * D; i += kAttnThreads)
+    for (int i = tid; i < G * D; i += NT)
         q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kvh * G) * D + i]) * a.qscale;
     {
         const uint32_t* rl_g = a.rl_loc + (size_t)b * a.Nmax + j0;
-        for (int i = tid; i < n; i += kAttnThreads) rl_s[i] = rl_g[i];
+        for (int i = tid; i < n; i += NT) rl_s[i] = rl_g[i];
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer
-        int issued = 0;
-        const uint32_t* rl = rl_s;
-        for (int it = 0; it < 2 * nst; ++it) {
-            if (*abort_flag) break;
-            const int stage = it % NST, round = it / NST;
-            if (round > 0) {
-                bool ok = mbar_wait_bounded(empty0 + 8 * stage, (round - 1) & 1);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) {
-                    *abort_flag = 1;
-                    atomicExch(a.err, 5 /* TKV_ETIMEOUT */);
-                    break;
-                }
+    // this warp's tiles: warp, warp + 4, ...; iterations 0..ntw-1 are K, ntw..2ntw-1 are V
+    const int ntw = warp < nst ? (nst - warp + kAttnWarps - 1) / kAttnWarps : 0;
+    const int total = 2 * ntw;
+    const uint8_t* k0v0 = reinterpret_cast<const uint8_t*>(a.k0v0);
+    const uint8_t* stg = reinterpret_cast<const uint8_t*>(a.stage);
+    auto issue = [&](int i) {
+        const int kv = i < ntw ? 0 : 1;
+        const int tile = warp + kAttnWarps * (i < ntw ? i : i - ntw);
+        const uint32_t dst0 = smem_u32(ring + (size_t)(i % kWarpStages) * C::sz_stage);
+        const int col = lane & 15;
+#pragma unroll 4
+        for (int rr = 0; rr < kRows / 2; ++rr) {
+            const int r = 2 * rr + (lane >> 4);
+            const int jl = tile * kRows + r;
+            if (jl >= n) break;
+            const uint32_t loc = rl_s[jl];
+            const int tier = loc_tier(loc), slot = loc_slot(loc);
+            const uint8_t* src;
+            int nbytes;
+            if (tier == 0) {
+                src = k0v0 + row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S0) * (2 * D);
+                nbytes = 2 * D;
+            } else if (tier == 1) {
+                src = stg + row_index(0, kv, b, kvh, slot, a.B, a.Hkv, a.S1) * (2 * D);
+                nbytes = 2 * D;
+            } else {
+                src = a.t2 + row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
+                nbytes = D + 16;
             }
-            const int kv = it < nst ? 0 : 1;
-            const int tile = it < nst ? it : it - nst;
-            const int jl = tile * kRows + lane;
-            uint32_t bytes = 0;
-            const void* src = nullptr;
-            bool fp8 = false;
-            if (jl < n) {
-                const uint32_t loc = rl[jl];
-                const int tier = loc_tier(loc), slot = loc_slot(loc);
-                if (tier == 0) {
-                    src = a.k0v0 + row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S0) * D;
-                    bytes = 2 * D;
-                } else if (tier == 1) {
-                    src = a.stage + row_index(0, kv, b, kvh, slot, a.B, a.Hkv, a.S1) * D;
-                    bytes = 2 * D;
-                } else {
-                    src = a.t2 + row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
-                    bytes = D + 16;
-                    fp8 = true;
-                }
-            }
-            const uint32_t mask = __ballot_sync(0xffffffffu, fp8);
-            const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
-            if (lane == 0) {
-                info[4 * stage] = mask;
-                info[4 * stage + 1] = (uint32_t)min(kRows, n - tile * kRows);
-                mbar_arrive_expect_tx(full0 + 8 * stage, total);
-            }
-            __syncwarp();
-            if (bytes) bulk_g2s(smem_u32(ring + (size_t)(stage * kRows + lane) * ROWB), src, bytes,
-                                full0 + 8 * stage);
-            issued = it + 1;
+            if (col * 16 < nbytes) cp_async16(dst0 + r * ROWB + col * 16, src + col * 16);
         }
-        // Leave no bulk copy in flight into this CTA's shared memory.
-        for (int it = max(0, issued - NST); it < issued; ++it)
-            (void)mbar_wait_bounded(full0 + 8 * (it % NST), (it / NST) & 1);
+    };
+
+#pragma unroll
+    for (int i = 0; i < kWarpStages - 1; ++i) {
+        if (i < total) issue(i);
+        cp_async_commit();
+    }
+
+    // ------------------------------------------------------------ pass 1: logits
+    float m_run[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) m_run[h] = -INFINITY;
+    for (int i = 0; i < ntw; ++i) {
+        if (i + kWarpStages - 1 < total) issue(i + kWarpStages - 1);
+        cp_async_commit();
+        cp_async_wait_prev();
         __syncwarp();
-    } else {
-        // ----------------------------------------------------------- consumers
-        float m_run[G];
+        const int tile = warp + kAttnWarps * i;
+        const int jl = tile * kRows + lane;
+        if (jl < n) {
+            const uint8_t* row = ring + (size_t)(i % kWarpStages) * C::sz_stage + (size_t)lane * ROWB;
+            const bool fp8 = loc_tier(rl_s[jl]) == 2;
+            // two independent accumulator pairs per head: (k0, k2) and (k1, k3) lanes of each chunk
+            float2 acc[G], acc2[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) m_run[h] = -INFINITY;
-
-        // pass 1: logits
-        for (int tile = warp; tile < nst; tile += kConsumerWarps) {
-            if (*abort_flag) break;
-            const int stage = tile % NST;
-            bool ok = mbar_wait_bounded(full0 + 8 * stage, (tile / NST) & 1);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                *abort_flag = 1;
-                atomicExch(a.err, 5);
-                break;
-            }
-            const uint32_t mask = info[4 * stage];
-            const int jl = tile * kRows + lane;
-            if (jl < n) {
-                const uint8_t* row = ring + (size_t)(stage * kRows + lane) * ROWB;
-                float2 acc[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
-                float zscale = 1.0f;
-                if (!((mask >> lane) & 1u)) {
+            for (int h = 0; h < G; ++h) acc[h] = acc2[h] = make_float2(0.f, 0.f);
+            float zscale = 1.0f;
+            if (!fp8) {
 #pragma unroll 4
-                    for (int c = 0; c < D / 8; ++c) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
-                        const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
-                        const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
+                    const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+                    const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
 #pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
-                            const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
-                            acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
-                            acc[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc[h]);
-                            acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
-                            acc[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc[h]);
-                        }
+                    for (int h = 0; h < G; ++h) {
+                        const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
+                        const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
+                        acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
+                        acc2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[h]);
+                        acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
+                        acc2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[h]);
                     }
-                } else {
-                    zscale = *reinterpret_cast<const float*>(row + D);
+                }
+            } else {
+                zscale = *reinterpret_cast<const float*>(row + D);
 #pragma unroll 4
-                    for (int c = 0; c < D / 8; ++c) {
-                        const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
-                        const float2 k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
-                        const float2 k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
-                        const float2 k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
-                        const float2 k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
+                    const float2 k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
+                    const float2 k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
+                    const float2 k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
+                    const float2 k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
 #pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
-                            const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
-                            acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
-                            acc[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc[h]);
-                            acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
-                            acc[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc[h]);
-                        }
+                    for (int h = 0; h < G; ++h) {
+                        const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
+                        const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
+                        acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
+                        acc2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[h]);
+                        acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
+                        acc2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[h]);
                     }
                 }
-                float z[GP];
-#pragma unroll
-                for (int h = 0; h < GP; ++h) z[h] = 0.f;
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    z[h] = (acc[h].x + acc[h].y) * zscale;
-                    m_run[h] = fmaxf(m_run[h], z[h]);
-                }
-#pragma unroll
-                for (int h = 0; h < GP; h += 4)
-                    *reinterpret_cast<float4*>(zp + (size_t)jl * GP + h) =
-                        make_float4(z[h], z[h + 1], z[h + 2], z[h + 3]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * stage);
-        }
-
-        // softmax statistics of this CTA's run
+            float z[GP];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float m = m_run[h];
+            for (int h = 0; h < GP; ++h) z[h] = 0.f;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0) wm[warp * 8 + h] = m;
-        }
-        named_bar_sync(1, kConsumerWarps * 32);
-        if (tid < G) {
-            float m = wm[tid];
-            for (int w = 1; w < kConsumerWarps; ++w) m = fmaxf(m, wm[w * 8 + tid]);
-            m_s[tid] = m;
-        }
-        named_bar_sync(1, kConsumerWarps * 32);
-        {
-            const int h = tid % GP;
-            float lsum = 0.f;
-            if (h < G) {
-                const float mh = m_s[h];
-                for (int idx = tid; idx < n * GP; idx += kConsumerWarps * 32) {
-                    const float p = exp2f(zp[idx] - mh);
-                    zp[idx] = p;
-                    lsum += p;
-                }
+            for (int h = 0; h < G; ++h) {
+                z[h] = ((acc[h].x + acc[h].y) + (acc2[h].x + acc2[h].y)) * zscale;
+                m_run[h] = fmaxf(m_run[h], z[h]);
             }
-            red[tid] = lsum;
-        }
-        named_bar_sync(1, kConsumerWarps * 32);
-        if (tid < G) {
-            float l = 0.f;
-            for (int k = tid; k < kConsumerWarps * 32; k += GP) l += red[k];
-            l_s[tid] = l;
-        }
-
-        // pass 2: values
-        float2 o[G][CPL / 2];
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int c = 0; c < CPL / 2; ++c) o[h][c] = make_float2(0.f, 0.f);
+            for (int h = 0; h < GP; h += 4)
+                *reinterpret_cast<float4*>(zp + (size_t)jl * GP + h) =
+                    make_float4(z[h], z[h + 1], z[h + 2], z[h + 3]);
+        }
+        __syncwarp();
+    }
 
-        for (int tile = warp; tile < nst; tile += kConsumerWarps) {
-            if (*abort_flag) break;
-            const int it = nst + tile;
-            const int stage = it % NST;
-            bool ok = mbar_wait_bounded(full0 + 8 * stage, (it / NST) & 1);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                *abort_flag = 1;
-                atomicExch(a.err, 5);
-                break;
+    // ------------------------------------------ softmax statistics of the run
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float m = m_run[h];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) wm[warp * 8 + h] = m;
+    }
+    __syncthreads();
+    if (tid < G) {
+        float m = wm[tid];
+        for (int w = 1; w < kAttnWarps; ++w) m = fmaxf(m, wm[w * 8 + tid]);
+        m_s[tid] = m;
+    }
+    __syncthreads();
+    {
+        const int h = tid % GP;
+        float lsum = 0.f;
+        if (h < G) {
+            const float mh = m_s[h];
+            for (int idx = tid; idx < n * GP; idx += NT) {
+                const float p = exp2f(zp[idx] - mh);
+                zp[idx] = p;
+                lsum += p;
             }
-            const uint32_t mask = info[4 * stage];
-            const int nrows = (int)info[4 * stage + 1];
-            for (int r = 0; r < nrows; ++r) {
-                const int jl = tile * kRows + r;
-                const uint8_t* row = ring + (size_t)(stage * kRows + r) * ROWB;
-                float p[GP];
+        }
+        red[tid] = lsum;
+    }
+    __syncthreads();
+    if (tid < G) {
+        float l = 0.f;
+        for (int k = tid; k < NT; k += GP) l += red[k];
+        l_s[tid] = l;
+    }
+
+    // ------------------------------------------------------------ pass 2: values
+    float2 o[G][CPL / 2];
 #pragma unroll
-                for (int h = 0; h < GP; h += 4) {
-                    const float4 t = *reinterpret_cast<const float4*>(zp + (size_t)jl * GP + h);
-                    p[h] = t.x; p[h + 1] = t.y; p[h + 2] = t.z; p[h + 3] = t.w;
-                }
-                float2 v[CPL / 2];
-                if (!((mask >> r) & 1u)) {
-                    if (CPL == 4) {
-                        const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
-                        v[0] = bf16x2_to_float2(w.x);
-                        v[CPL / 2 - 1] = bf16x2_to_float2(w.y);
-                    } else {
-                        v[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + lane * 4));
-                    }
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int c = 0; c < CPL / 2; ++c) o[h][c] = make_float2(0.f, 0.f);
+    for (int i = ntw; i < total; ++i) {
+        if (i + kWarpStages - 1 < total) issue(i + kWarpStages - 1);
+        cp_async_commit();
+        cp_async_wait_prev();
+        __syncwarp();
+        const int tile = warp + kAttnWarps * (i - ntw);
+        const int nrows = min(kRows, n - tile * kRows);
+        const uint8_t* stage = ring + (size_t)(i % kWarpStages) * C::sz_stage;
+        for (int r = 0; r < nrows; ++r) {
+            const int jl = tile * kRows + r;
+            const uint8_t* row = stage + (size_t)r * ROWB;
+            float p[GP];
+#pragma unroll
+            for (int h = 0; h < GP; h += 4) {
+                const float4 t = *reinterpret_cast<const float4*>(zp + (size_t)jl * GP + h);
+                p[h] = t.x; p[h + 1] = t.y; p[h + 2] = t.z; p[h + 3] = t.w;
+            }
+            float2 v[CPL / 2];
+            if (loc_tier(rl_s[jl]) != 2) {
+                if (CPL == 4) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
+                    v[0] = bf16x2_to_float2(w.x);
+                    v[CPL / 2 - 1] = bf16x2_to_float2(w.y);
                 } else {
-                    const float sc = *reinterpret_cast<const float*>(row + D);
-#pragma unroll
-                    for (int h = 0; h < G; ++h) p[h] *= sc;
-                    if (CPL == 4) {
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
-                        v[0] = e4m3x2_to_float2((uint16_t)(w & 0xFFFF));
-                        v[CPL / 2 - 1] = e4m3x2_to_float2((uint16_t)(w >> 16));
-                    } else {
-                        v[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(row + lane * 2));
-                    }
+                    v[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + lane * 4));
                 }
+            } else {
+                const float sc = *reinterpret_cast<const float*>(row + D);
 #pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int c = 0; c < CPL / 2; ++c)
-                        o[h][c] = __ffma2_rn(make_float2(p[h], p[h]), v[c], o[h][c]);
+                for (int h = 0; h < G; ++h) p[h] *= sc;
+                if (CPL == 4) {
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
+                    v[0] = e4m3x2_to_float2((uint16_t)(w & 0xFFFF));
+                    v[CPL / 2 - 1] = e4m3x2_to_float2((uint16_t)(w >> 16));
+                } else {
+                    v[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(row + lane * 2));
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int c = 0; c < CPL / 2; ++c)
+                    o[h][c] = __ffma2_rn(make_float2(p[h], p[h]), v[c], o[h][c]);
         }
+        __syncwarp();
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
 
-        // combine the four warps' partial O (fixed order); the ring is free now
-        named_bar_sync(1, kConsumerWarps * 32);
+    // combine the warps' partial O (fixed order); each warp's ring is free now
+    {
         float* ored = reinterpret_cast<float*>(ring);
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
             for (int c = 0; c < CPL / 2; ++c)
-                *reinterpret_cast<float2*>(ored + ((size_t)warp * G + h) * D + lane * CPL + 2 * c) =
-                    o[h][c];
-        named_bar_sync(1, kConsumerWarps * 32);
-        for (int i = tid; i < G * D; i += kConsumerWarps * 32) {
-            float acc = ored[i];
-            for (int w = 1; w < kConsumerWarps; ++w) acc += ored[(size_t)w * G * D + i];
-            o_s[i] = acc;
-        }
+                *reinterpret_cast<float2*>(ored + (size_t)h * D + lane * CPL + 2 * c) = o[h][c];
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += NT) {
+        float acc = 0.f;
+        for (int w = 0; w < kAttnWarps; ++w)
+            acc += reinterpret_cast<const float*>(smem + C::off_ring + (size_t)w * C::sz_warp_ring)[i];
+        o_s[i] = acc;
     }
 
     // ------------------------------------------------------------ cluster merge
     cluster_sync_all();
+    if (tid < kMaxSplits * 8) {
+        const int r = tid >> 3, h = tid & 7;
+        if (r < S && h < G) {
+            mall[tid] = dsmem_ld_f32(dsmem_addr(smem_u32(m_s + h), r));
+            lall[tid] = dsmem_ld_f32(dsmem_addr(smem_u32(l_s + h), r));
+        }
+    }
+    __syncthreads();
     if (tid < G) {
         const int h = tid;
-        const uint32_t am = smem_u32(m_s + h), al = smem_u32(l_s + h);
         float M = -INFINITY;
-        for (int r = 0; r < S; ++r) M = fmaxf(M, dsmem_ld_f32(dsmem_addr(am, r)));
+        for (int r = 0; r < S; ++r) M = fmaxf(M, mall[r * 8 + h]);
         float Lsum = 0.f;
         for (int r = 0; r < S; ++r) {
-            const float mr = dsmem_ld_f32(dsmem_addr(am, r));
+            const float mr = mall[r * 8 + h];
             const float e = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
             f_s[r * 8 + h] = e;
-            Lsum += dsmem_ld_f32(dsmem_addr(al, r)) * e;
+            Lsum += lall[r * 8 + h] * e;
         }
         const float inv = 1.0f / Lsum;
         for (int r = 0; r < S; ++r) f_s[r * 8 + h] *= inv;
@@ -377,7 +368,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 #pragma unroll
         for (int h = 0; h < G; ++h) f_self[h] = f_s[rank * 8 + h];
         float* gdst = a.g + (((size_t)a.layer * a.B + b) * a.Hkv + kvh) * a.Nmax + j0;
-        for (int jl = tid; jl < n; jl += kAttnThreads) {
+        for (int jl = tid; jl < n; jl += NT) {
             float acc = 0.f;
 #pragma unroll
             for (int h = 0; h < G; ++h) acc += zp[(size_t)jl * GP + h] * f_self[h];
@@ -390,10 +381,16 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         const int per = (G * D + S - 1) / S;
         const int i0 = rank * per, i1 = min(G * D, i0 + per);
         const uint32_t ao = smem_u32(o_s);
-        for (int i = i0 + tid; i < i1; i += kAttnThreads) {
+        for (int i = i0 + tid; i < i1; i += NT) {
             const int h = i / D, c = i % D;
+            float v[kMaxSplits];
+#pragma unroll
+            for (int r = 0; r < kMaxSplits; ++r)
+                v[r] = (r < S) ? dsmem_ld_f32(dsmem_addr(ao + 4u * i, r)) : 0.f;
             float acc = 0.f;
-            for (int r = 0; r < S; ++r) acc += dsmem_ld_f32(dsmem_addr(ao + 4u * i, r)) * f_s[r * 8 + h];
+#pragma unroll
+            for (int r = 0; r < kMaxSplits; ++r)
+                if (r < S) acc += v[r] * f_s[r * 8 + h];
             a.out[((size_t)b * a.Hq + (size_t)kvh * G + h) * D + c] = acc;
         }
     }
@@ -406,7 +403,7 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
     const size_t smem = AttnCfg<G, D>::smem(a.chunk);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.splits, a.Hkv, a.B);
-    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -431,7 +428,7 @@ template <int G, int D>
 static bool cluster_fits_gd(size_t smem, int s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(s, 1, 1);
-    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -400,6 +400,44 @@ cudaError_t launch_moves(const MoveArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ T1 copy kernel
+// SM-driven copy of the per-layer T1 rows from pinned host memory (zero-copy
+// loads over the host link) into HBM staging; four independent 16-byte loads
+// in flight per thread.
+__global__ void __launch_bounds__(256) t1_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                      size_t pitch16, size_t width16, int row_begin,
+                                                      int row_end) {
+    const size_t total = (size_t)(row_end - row_begin) * width16;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; e + 3 * stride < total; e += 4 * stride) {
+        uint4 w[4];
+        size_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const size_t x = e + k * stride;
+            o[k] = (size_t)(row_begin + x / width16) * pitch16 + x % width16;
+            w[k] = src[o[k]];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[o[k]] = w[k];
+    }
+    for (; e < total; e += stride) {
+        const size_t o = (size_t)(row_begin + e / width16) * pitch16 + e % width16;
+        dst[o] = src[o];
+    }
+}
+
+cudaError_t launch_t1_copy(const void* src, void* dst, size_t pitch16, size_t width16, int row_begin,
+                           int row_end, cudaStream_t st) {
+    if (row_end <= row_begin || width16 == 0) return cudaSuccess;
+    const size_t total = (size_t)(row_end - row_begin) * width16;
+    const int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
+    t1_copy_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
+                                           pitch16, width16, row_begin, row_end);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------ open / append
 // Opens n new positions [N, N+n) of every sequence in T0: pops T0 slots from
 // the free stack, resets s, appends to the retained list.

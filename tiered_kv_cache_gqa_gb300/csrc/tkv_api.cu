@@ -25,8 +25,9 @@ struct tkv_ctx {
     int L = 0, B = 0, Hq = 0, Hkv = 0, G = 0, d = 0, Nmax = 0, S0 = 0, S1 = 0, S2 = 0;
     int64_t ppm[4] = {0, 0, 0, 0};
     int device = 0;
-    cudaStream_t compute = nullptr, copy = nullptr;
+    cudaStream_t compute = nullptr, copy = nullptr, copy2 = nullptr;
     bool own_compute = false, own_copy = false;
+    cudaEvent_t ev_split = nullptr;
 
     // device
     __nv_bfloat16* k0v0 = nullptr;
@@ -166,6 +167,8 @@ void free_all(tkv_ctx* c) {
         for (cudaEvent_t e : v) cudaEventDestroy(e);
     if (c->own_compute && c->compute) cudaStreamDestroy(c->compute);
     if (c->own_copy && c->copy) cudaStreamDestroy(c->copy);
+    if (c->copy2) cudaStreamDestroy(c->copy2);
+    if (c->ev_split) cudaEventDestroy(c->ev_split);
     (void)cudaGetLastError();
 }
 
@@ -307,11 +310,28 @@ tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
         const size_t pitch = (size_t)ctx->S1 * ctx->d * sizeof(__nv_bfloat16);
         const size_t layer_elems = (size_t)2 * ctx->B * ctx->Hkv * ctx->S1 * ctx->d;
         const __nv_bfloat16* src = ctx->h1 + (size_t)layer * layer_elems;
+        const __nv_bfloat16* dsrc = ctx->d_h1 + (size_t)layer * layer_elems;
         __nv_bfloat16* dst = ctx->stage + (size_t)slotr * layer_elems;
         const size_t width = (size_t)ctx->hw1 * ctx->d * sizeof(__nv_bfloat16);
-        const size_t height = (size_t)2 * ctx->B * ctx->Hkv;
+        const int height = 2 * ctx->B * ctx->Hkv;
+        const int mode = ctx->cfg.t1_transport;
+        // rows [0, h_ce) by the copy engine, [h_ce, height) by the copy kernel
+        const int h_ce = mode == TKV_T1_COPY_ENGINE ? height : mode == TKV_T1_SM_COPY ? 0 : height / 2;
         const bool timed = prof_open(ctx, 1, ctx->copy);
-        CK(cudaMemcpy2DAsync(dst, pitch, src, pitch, width, height, cudaMemcpyHostToDevice, ctx->copy));
+        if (h_ce < height) {
+            cudaStream_t ks = ctx->copy;
+            if (h_ce > 0) {
+                ks = ctx->copy2;
+                CK(cudaStreamWaitEvent(ks, ctx->ev_attn[slotr], 0));
+                CK(cudaStreamWaitEvent(ks, ctx->ev_retier, 0));
+            }
+            CK(launch_t1_copy(dsrc, dst, pitch / 16, width / 16, h_ce, height, ks));
+            ctx->launches++;
+            if (h_ce > 0) CK(cudaEventRecord(ctx->ev_split, ks));
+        }
+        if (h_ce > 0)
+            CK(cudaMemcpy2DAsync(dst, pitch, src, pitch, width, h_ce, cudaMemcpyHostToDevice, ctx->copy));
+        if (h_ce > 0 && h_ce < height) CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_split, 0));
         if (timed) prof_close(ctx, 1, ctx->copy, (double)(width * height));
         ctx->st.h2d_bytes_t1_stream += (int64_t)(width * height);
     }
@@ -352,6 +372,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     if (c.max_tokens < 1 || c.max_tokens > 65536) return TKV_EINVAL;
     if (c.prompt_len < 0 || c.num_sinks < 0 || c.recent_window < 0) return TKV_EINVAL;
     if (c.t0_capacity < 0 || c.t1_capacity < 0 || c.t2_capacity < 0) return TKV_EINVAL;
+    if (c.t1_transport < TKV_T1_COPY_ENGINE || c.t1_transport > TKV_T1_SPLIT) return TKV_EINVAL;
     const float r[4] = {c.ratio_t0, c.ratio_t1, c.ratio_t2, c.ratio_t3};
     int64_t ppm[4], sum = 0;
     for (int i = 0; i < 4; ++i) {
@@ -461,6 +482,8 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
         E(cudaEventCreateWithFlags(&ctx->ev_attn[i], cudaEventDisableTiming));
     }
     E(cudaEventCreateWithFlags(&ctx->ev_retier, cudaEventDisableTiming));
+    E(cudaEventCreateWithFlags(&ctx->ev_split, cudaEventDisableTiming));
+    E(cudaStreamCreateWithFlags(&ctx->copy2, cudaStreamNonBlocking));
     if (!e) {
         (void)cudaGetLastError();
         return bail(TKV_ECUDA);

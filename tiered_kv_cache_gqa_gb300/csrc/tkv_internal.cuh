@@ -22,10 +22,7 @@
 namespace tkv {
 
 constexpr int kMaxSplits = 16;          // CTAs per (sequence, KV head) cluster
-constexpr int kRows = 32;               // rows per pipeline stage
-constexpr int kConsumerWarps = 4;
-constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
-constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz: bound of every device wait
+constexpr int kRows = 32;               // rows per pipeline tile
 
 // Move kinds produced by a re-tier.
 enum MoveKind : int {
@@ -71,56 +68,6 @@ __host__ __device__ inline size_t row_index(int layer, int kv, int b, int h, int
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(
-                     bar),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for the phase with the given parity to complete, at most kWaitCycles.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    long long t0 = clock64();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitCycles) return false;
-    }
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -176,7 +123,7 @@ struct AttnArgs {
     const uint32_t* rl_loc;      // [B][Nmax]
     const int32_t* rl_count;     // [B]
     float* g;                    // [L][B][Hkv][Nmax]
-    int32_t* err;
+    int32_t* err;                // status word (unused by kernels without device waits)
     int layer, L, B, Hq, Hkv, d, Nmax, S0, S1, S2;
     int splits, chunk;           // CTAs per (b, kv head) and retained rows per CTA
     float qscale;                // log2(e) / sqrt(d)
@@ -239,5 +186,10 @@ struct MoveArgs {
 };
 
 cudaError_t launch_moves(const MoveArgs& a, cudaStream_t st);
+
+// Copies rows [row_begin, row_end) of a pitched 2-D region (16-byte units):
+// dst[r * pitch16 + c] = src[r * pitch16 + c] for c < width16.
+cudaError_t launch_t1_copy(const void* src, void* dst, size_t pitch16, size_t width16, int row_begin,
+                           int row_end, cudaStream_t st);
 
 }  // namespace tkv
