@@ -118,7 +118,7 @@ typedef struct {
     int64_t kv_bytes_full_cache;   /* bf16 KV bytes of all N positions (no tiering) */
     int64_t kernel_launches;       /* kernels this context has launched (all kinds) */
     int32_t status;                /* tkv_status of the context */
-    int32_t attn_splits;           /* CTAs per (sequence, KV head) of the last attention launch */
+    int32_t attn_splits;           /* CTAs of the last attention launch */
 } tkv_stats;
 
 /* Creates a context: device pools for T0 (bf16), T2 (fp8 + scales) and the
@@ -251,9 +251,10 @@ tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t
  *   s:   device fp32 [B][R], read and updated in place: s += the step's mean
  *        over layers and query heads of the attention weights
  *   stream: cudaStream_t to enqueue on (NULL = the legacy default stream)
- * Scratch lives in fixed file-scope device arrays, held by every GPU that
- * loads the library until exit: L*B*Hkv*R <= 2,097,152, B*R <= 262,144,
- * B <= 256; larger sizes return TKV_ECAPACITY before anything is enqueued.
+ * Scratch lives in fixed file-scope device arrays (about 22 MiB), held by
+ * every GPU that loads the library until exit: L*B*Hkv*R <= 1,048,576,
+ * B*Hkv*R <= 131,072, B*R <= 131,072, B <= 256; larger sizes return
+ * TKV_ECAPACITY before anything is enqueued.
  * It calls no cudaMalloc, cudaFree or other allocating routine.  The first
  * call on a device (with that device current) resolves the scratch addresses
  * and should come before any stream capture.  All calls share the scratch and

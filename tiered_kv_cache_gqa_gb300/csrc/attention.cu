@@ -1,5 +1,5 @@
-// Decode attention over the tiered KV cache, with fused emission of the
-// per-position attention-weight sums, and the score fold.
+// Decode attention over the tiered KV cache, with the per-position sums of
+// the attention weights that feed the score update, and the score fold.
 //
 // Method: "Not All Thoughts Need HBM" (gist.science summary), sections
 // "Zero-approximation-error offloading" (T1 rows take part at full precision;
@@ -8,71 +8,62 @@
 // "Tri-state cache assignment" (8-bit rows are dequantised on the fly and taken
 // in their original order).
 //
-// One thread-block cluster per (sequence b, KV head); its `splits` CTAs each
-// own a contiguous run of the retained list (positions in logical order).  The
-// run length depends only on the number of retained positions, never on which
-// tier a row sits in, and every sum below has a fixed order, so a row read
-// from T0 or from the T1 staging ring gives bit-identical results.
-//
-// Per CTA, four warps.  A warp owns the tiles w, w+4, ... (32 rows each) of the
-// CTA's run; it streams the K rows of its tiles, then their V rows, through its
-// own two-stage shared-memory ring with cp.async (16 bytes per lane, 16 lanes
-// per 256-byte row, each row fetched from its home: T0 pool, T1 staging or T2
-// pool), so loads for the next tile are in flight while the current one is
-// computed.  The only waits are cp.async.wait_group and hardware barriers.
-//   pass 1 (K): lane = row; z[h] = q'_h . k for the G query heads of the
-//              group, with q' = q * log2(e)/sqrt(d) in shared memory
-//              (broadcast reads) and packed f32x2 FMAs; z is kept in shared
-//              memory; T2 rows: z = scale * (q' . code values).
-//   softmax:   per-CTA max m_h over the run, p = 2^(z - m_h) in place,
-//              l_h = sum p (fixed-order reduction).
-//   pass 2 (V): the warp walks its tiles' rows; lane = 4 (or 2) columns;
-//              O_h += p * v.
-// Cluster merge (distributed shared memory): every CTA gathers all peers'
-// (m, l) -> M_h, L_h, per-peer factors f_r = 2^(m_r - M)/L; it writes, for its
-// own rows, g[j] = sum_h p_h[j] * f_self,h (the sum over the group's query
-// heads of alpha), and reduces its share of O over the peers in rank order.
-// No atomics touch `out` or `g`.
+// Work split.  The retained list of every (sequence b, KV head) group is cut
+// into items of `item_rows` consecutive positions.  The main kernel runs
+// persistent CTAs of four warps; CTA c owns a contiguous range of items in
+// (b, KV head, item) order.  Within an item, warp w owns the 32-row tiles w and
+// w + 4.  Each warp streams, item after item, the K rows and then the V rows
+// of its tiles through its own two-stage shared-memory ring with 16-byte
+// cp.async (16 lanes per 256-byte row, every row fetched from its home: T0
+// pool, T1 staging or T2 pool), so the next tile -- possibly of the next item --
+// is in flight while the current one is computed.  The only waits are
+// cp.async.wait_group and CTA barriers; there are no spin loops.
+//   K tile:  lane = row; z_h = q'_h . k for the G query heads of the group,
+//            q' = q * log2(e)/sqrt(d) in shared memory (broadcast reads),
+//            packed f32x2 FMAs; T2 rows: z = scale * (q' . code values).
+//   stats:   per warp and item, m_h = max z, p = 2^(z - m_h), l_h = sum p;
+//            z goes to a global scratch for the alpha sums.
+//   V tile:  the warp walks the tile's rows, lane = 4 (or 2) columns,
+//            O_h += p * v.
+//   item end: the four warps' (m, l, O) are merged in shared memory (fixed
+//            order) into the item's partial, written to global scratch.
+// The combine kernel then merges a group's item partials in item order into
+// `out`, and writes per position g = sum_h 2^(z_h - M_h) / L_h (the sum over the
+// group's query heads of alpha).  Item boundaries, the CTA ranges and every
+// reduction order depend only on the retained counts, never on which tier a
+// row sits in, so a row read from T0 or from the T1 staging ring gives
+// bit-identical results.  No atomics touch `out` or `g`.
+#include <algorithm>
 #include <cmath>
 
 #include "tkv_internal.cuh"
 
 namespace tkv {
 
-#ifndef TKV_ATTN_WARPS
-#define TKV_ATTN_WARPS 4
-#endif
-#ifndef TKV_WARP_STAGES
-#define TKV_WARP_STAGES 2
-#endif
-constexpr int kAttnWarps = TKV_ATTN_WARPS;     // warps per CTA
-constexpr int kWarpStages = TKV_WARP_STAGES;   // ring stages per warp
+constexpr int kAttnWarps = 4;
+constexpr int kWarpStages = 2;
+constexpr int kMaxWindowRows = 4096;       // retained-list rows a CTA stages in shared memory
+constexpr int kCombineRows = 1024;         // rows per combine block
 
 template <int G, int D>
 struct AttnCfg {
     static constexpr int GP = (G <= 4) ? 4 : 8;      // z / p row stride (floats)
     static constexpr int ROWB = 2 * D + 16;          // ring row stride (bytes), bank-skewed
-    static constexpr int CPL = D / 32;               // pass-2 columns per lane
+    static constexpr int CPL = D / 32;               // V columns per lane
     static_assert(D == 64 || D == 128, "head_dim must be 64 or 128");
     static_assert(G >= 1 && G <= 8, "group size must be 1..8");
 
     static constexpr size_t sz_stage = (size_t)kRows * ROWB;
     static constexpr size_t sz_warp_ring = kWarpStages * sz_stage;
+    static constexpr int PS = 16 + G * D;            // floats of one (m[8], l[8], O[G][D]) record
     static constexpr size_t off_ring = 0;
     static constexpr size_t off_q = kAttnWarps * sz_warp_ring;
-    static constexpr size_t off_o = off_q;   // O is written after q's last use
-    static constexpr size_t off_m = off_q + (size_t)G * D * 4;
-    static constexpr size_t off_l = off_m + 32;
-    static constexpr size_t off_f = off_l + 32;
-    static constexpr size_t off_mall = off_f + (size_t)kMaxSplits * 8 * 4;
-    static constexpr size_t off_lall = off_mall + (size_t)kMaxSplits * 8 * 4;
-    static constexpr size_t off_red = off_lall + (size_t)kMaxSplits * 8 * 4;
-    static constexpr size_t off_wm = off_red + kAttnWarps * 32 * 4;
-    static constexpr size_t off_zp = off_wm + kAttnWarps * 8 * 4;
-    static_assert((size_t)G * D * 4 <= sz_warp_ring, "a warp's partial O reuses its ring");
+    static constexpr size_t off_p = off_q + (size_t)G * D * 4;
+    static constexpr size_t off_comb = off_p + (size_t)kAttnWarps * kRows * GP * 4;
+    static constexpr size_t off_n = off_comb + (size_t)kAttnWarps * PS * 4;   // rows of each item
+    static constexpr size_t off_rl = off_n + (size_t)(kMaxWindowRows / 128) * 4;
 
-    // then z/p (chunk x GP floats) and the CTA's slice of the retained list (chunk u32)
-    static size_t smem(int chunk) { return off_zp + (size_t)chunk * GP * 4 + (size_t)chunk * 4; }
+    static size_t smem(int rl_rows) { return off_rl + (size_t)rl_rows * 4; }
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -84,363 +75,450 @@ __device__ __forceinline__ void cp_async_wait_prev() {
 }
 
 template <int G, int D>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
-    constexpr int GP = C::GP, ROWB = C::ROWB, CPL = C::CPL;
+    constexpr int GP = C::GP, ROWB = C::ROWB, CPL = C::CPL, PS = C::PS;
     constexpr int NT = kAttnWarps * 32;
     extern __shared__ __align__(128) uint8_t smem[];
     float* q_s = reinterpret_cast<float*>(smem + C::off_q);
-    float* o_s = reinterpret_cast<float*>(smem + C::off_o);
-    float* m_s = reinterpret_cast<float*>(smem + C::off_m);
-    float* l_s = reinterpret_cast<float*>(smem + C::off_l);
-    float* f_s = reinterpret_cast<float*>(smem + C::off_f);
-    float* mall = reinterpret_cast<float*>(smem + C::off_mall);
-    float* lall = reinterpret_cast<float*>(smem + C::off_lall);
-    float* red = reinterpret_cast<float*>(smem + C::off_red);
-    float* wm = reinterpret_cast<float*>(smem + C::off_wm);
-    float* zp = reinterpret_cast<float*>(smem + C::off_zp);
-    uint32_t* rl_s = reinterpret_cast<uint32_t*>(smem + C::off_zp + (size_t)a.chunk * GP * 4);
+    float* comb = reinterpret_cast<float*>(smem + C::off_comb);
+    uint32_t* rl_s = reinterpret_cast<uint32_t*>(smem + C::off_rl);
+    int* n_s = reinterpret_cast<int*>(smem + C::off_n);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rank = (int)cluster_rank();
-    const int kvh = blockIdx.y, b = blockIdx.z;
-    const int S = a.splits;
-    const int R = a.rl_count[b];
-    const int j0 = rank * a.chunk;
-    const int n = max(0, min(R, j0 + a.chunk) - j0);
-    const int nst = (n + kRows - 1) / kRows;
+    const int IT = a.item_rows, IPG = a.items_per_group;
+    const int total_items = a.B * a.Hkv * IPG;
+    const int it0 = blockIdx.x * a.items_per_cta;
+    const int it1 = min(total_items, it0 + a.items_per_cta);
+    if (it0 >= it1) return;
+    const int g_first = it0 / IPG;
     uint8_t* ring = smem + C::off_ring + (size_t)warp * C::sz_warp_ring;
+    float* p_s = reinterpret_cast<float*>(smem + C::off_p) + (size_t)warp * kRows * GP;
 
-    for (int i = tid; i < G * D; i += NT)
-        q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kvh * G) * D + i]) * a.qscale;
-    {
-        const uint32_t* rl_g = a.rl_loc + (size_t)b * a.Nmax + j0;
-        for (int i = tid; i < n; i += NT) rl_s[i] = rl_g[i];
+    // rows of every item of this CTA, and their retained-list slices
+    for (int item = it0 + tid; item < it1; item += NT) {
+        const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
+        n_s[item - it0] = max(0, min(IT, a.rl_count[b] - j0));
     }
     __syncthreads();
+    for (int item = it0; item < it1; ++item) {
+        const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
+        const int n = n_s[item - it0];
+        const uint32_t* src = a.rl_loc + (size_t)b * a.Nmax + j0;
+        uint32_t* dst = rl_s + (size_t)(item - it0) * IT;
+        for (int r = tid; r < n; r += NT) dst[r] = src[r];
+    }
+    __syncthreads();
+    // tiles of this warp in an item: warp, warp + 4, ... below ceil(n / 32)
+    auto warp_tiles = [&](int n) {
+        const int nt = (n + kRows - 1) / kRows;
+        return warp < nt ? (nt - warp + kAttnWarps - 1) / kAttnWarps : 0;
+    };
 
-    // this warp's tiles: warp, warp + 4, ...; iterations 0..ntw-1 are K, ntw..2ntw-1 are V
-    const int ntw = warp < nst ? (nst - warp + kAttnWarps - 1) / kAttnWarps : 0;
-    const int total = 2 * ntw;
+    // ------------------------------------------------------------ issue side
+    // Sequence per warp: for every item, for every tile of this warp: K tile, V tile.
+    int ci_item = it0, ci_k = 0, ci_kv = 0, issued = 0;
+    auto settle = [&]() {
+        while (ci_item < it1 && warp_tiles(n_s[ci_item - it0]) == 0) ++ci_item;
+    };
+    settle();
     const uint8_t* k0v0 = reinterpret_cast<const uint8_t*>(a.k0v0);
     const uint8_t* stg = reinterpret_cast<const uint8_t*>(a.stage);
-    auto issue = [&](int i) {
-        const int kv = i < ntw ? 0 : 1;
-        const int tile = warp + kAttnWarps * (i < ntw ? i : i - ntw);
-        const uint32_t dst0 = smem_u32(ring + (size_t)(i % kWarpStages) * C::sz_stage);
-        const int col = lane & 15;
-#pragma unroll 4
-        for (int rr = 0; rr < kRows / 2; ++rr) {
-            const int r = 2 * rr + (lane >> 4);
-            const int jl = tile * kRows + r;
-            if (jl >= n) break;
-            const uint32_t loc = rl_s[jl];
-            const int tier = loc_tier(loc), slot = loc_slot(loc);
-            const uint8_t* src;
-            int nbytes;
-            if (tier == 0) {
-                src = k0v0 + row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S0) * (2 * D);
-                nbytes = 2 * D;
-            } else if (tier == 1) {
-                src = stg + row_index(0, kv, b, kvh, slot, a.B, a.Hkv, a.S1) * (2 * D);
-                nbytes = 2 * D;
-            } else {
-                src = a.t2 + row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
-                nbytes = D + 16;
+    // the lane's row of the tile being issued: K address, V address, byte count
+    const uint8_t* row_v = nullptr;
+    int row_bytes = 0;
+    uint32_t fp8_mask_issue = 0;       // T2 rows of the tile last issued as K
+    auto issue_next = [&]() {
+        if (ci_item >= it1) return;
+        const int item = ci_item, kv = ci_kv;
+        const int n = n_s[item - it0];
+        const int tile = warp + kAttnWarps * ci_k;
+        const int jl = tile * kRows + lane;
+        if (kv == 0) {
+            const int g = item / IPG, b = g / a.Hkv, kvh = g % a.Hkv;
+            const uint8_t* row_k = nullptr;
+            row_bytes = 0;
+            bool fp8 = false;
+            if (jl < n) {
+                const uint32_t loc = rl_s[(size_t)(item - it0) * IT + jl];
+                const int tier = loc_tier(loc);
+                const size_t slot = (size_t)loc_slot(loc);
+                if (tier == 0) {
+                    row_k = k0v0 + row_index(a.layer, 0, b, kvh, (int)slot, a.B, a.Hkv, a.S0) * (2 * D);
+                    row_v = k0v0 + row_index(a.layer, 1, b, kvh, (int)slot, a.B, a.Hkv, a.S0) * (2 * D);
+                    row_bytes = 2 * D;
+                } else if (tier == 1) {
+                    row_k = stg + row_index(0, 0, b, kvh, (int)slot, a.B, a.Hkv, a.S1) * (2 * D);
+                    row_v = stg + row_index(0, 1, b, kvh, (int)slot, a.B, a.Hkv, a.S1) * (2 * D);
+                    row_bytes = 2 * D;
+                } else {
+                    row_k = a.t2 + row_index(a.layer, 0, b, kvh, (int)slot, a.B, a.Hkv, a.S2) * (D + 16);
+                    row_v = a.t2 + row_index(a.layer, 1, b, kvh, (int)slot, a.B, a.Hkv, a.S2) * (D + 16);
+                    row_bytes = D + 16;
+                    fp8 = true;
+                }
             }
-            if (col * 16 < nbytes) cp_async16(dst0 + r * ROWB + col * 16, src + col * 16);
+            fp8_mask_issue = __ballot_sync(0xffffffffu, fp8);
+            const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * C::sz_stage);
+            const int col = lane & 15, half = lane >> 4;
+#pragma unroll 4
+            for (int rr = 0; rr < kRows / 2; ++rr) {
+                const int r = 2 * rr + half;
+                const uint8_t* src = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)row_k, r);
+                const int nb = __shfl_sync(0xffffffffu, row_bytes, r);
+                if (col * 16 < nb) cp_async16(dst0 + r * ROWB + col * 16, src + col * 16);
+            }
+        } else {
+            const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * C::sz_stage);
+            const int col = lane & 15, half = lane >> 4;
+#pragma unroll 4
+            for (int rr = 0; rr < kRows / 2; ++rr) {
+                const int r = 2 * rr + half;
+                const uint8_t* src = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)row_v, r);
+                const int nb = __shfl_sync(0xffffffffu, row_bytes, r);
+                if (col * 16 < nb) cp_async16(dst0 + r * ROWB + col * 16, src + col * 16);
+            }
+        }
+        ++issued;
+        if (ci_kv == 0) {
+            ci_kv = 1;
+        } else {
+            ci_kv = 0;
+            if (++ci_k >= warp_tiles(n)) {
+                ci_k = 0;
+                ++ci_item;
+                settle();
+            }
         }
     };
 
-#pragma unroll
-    for (int i = 0; i < kWarpStages - 1; ++i) {
-        if (i < total) issue(i);
-        cp_async_commit();
-    }
+    issue_next();
+    cp_async_commit();
+    int consumed = 0;
 
-    // ------------------------------------------------------------ pass 1: logits
-    float m_run[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) m_run[h] = -INFINITY;
-    for (int i = 0; i < ntw; ++i) {
-        if (i + kWarpStages - 1 < total) issue(i + kWarpStages - 1);
-        cp_async_commit();
-        cp_async_wait_prev();
-        __syncwarp();
-        const int tile = warp + kAttnWarps * i;
-        const int jl = tile * kRows + lane;
-        if (jl < n) {
-            const uint8_t* row = ring + (size_t)(i % kWarpStages) * C::sz_stage + (size_t)lane * ROWB;
-            const bool fp8 = loc_tier(rl_s[jl]) == 2;
-            // two independent accumulator pairs per head: (k0, k2) and (k1, k3) lanes of each chunk
-            float2 acc[G], acc2[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = acc2[h] = make_float2(0.f, 0.f);
-            float zscale = 1.0f;
-            if (!fp8) {
-#pragma unroll 4
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
-                    const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
-                    const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
-                        const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
-                        acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
-                        acc2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[h]);
-                        acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
-                        acc2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[h]);
-                    }
-                }
-            } else {
-                zscale = *reinterpret_cast<const float*>(row + D);
-#pragma unroll 4
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
-                    const float2 k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
-                    const float2 k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
-                    const float2 k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
-                    const float2 k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
-                        const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
-                        acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
-                        acc2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[h]);
-                        acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
-                        acc2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[h]);
-                    }
-                }
-            }
-            float z[GP];
-#pragma unroll
-            for (int h = 0; h < GP; ++h) z[h] = 0.f;
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                z[h] = ((acc[h].x + acc[h].y) + (acc2[h].x + acc2[h].y)) * zscale;
-                m_run[h] = fmaxf(m_run[h], z[h]);
-            }
-#pragma unroll
-            for (int h = 0; h < GP; h += 4)
-                *reinterpret_cast<float4*>(zp + (size_t)jl * GP + h) =
-                    make_float4(z[h], z[h + 1], z[h + 2], z[h + 3]);
-        }
-        __syncwarp();
-    }
-
-    // ------------------------------------------ softmax statistics of the run
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float m = m_run[h];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0) wm[warp * 8 + h] = m;
-    }
-    __syncthreads();
-    if (tid < G) {
-        float m = wm[tid];
-        for (int w = 1; w < kAttnWarps; ++w) m = fmaxf(m, wm[w * 8 + tid]);
-        m_s[tid] = m;
-    }
-    __syncthreads();
-    {
-        const int h = tid % GP;
-        float lsum = 0.f;
-        if (h < G) {
-            const float mh = m_s[h];
-            for (int idx = tid; idx < n * GP; idx += NT) {
-                const float p = exp2f(zp[idx] - mh);
-                zp[idx] = p;
-                lsum += p;
-            }
-        }
-        red[tid] = lsum;
-    }
-    __syncthreads();
-    if (tid < G) {
-        float l = 0.f;
-        for (int k = tid; k < NT; k += GP) l += red[k];
-        l_s[tid] = l;
-    }
-
-    // ------------------------------------------------------------ pass 2: values
+    // ---------------------------------------------------- per-warp segment state
+    float m_w[G], l_l[G];
     float2 o[G][CPL / 2];
+    auto reset_segment = [&]() {
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+        for (int h = 0; h < G; ++h) {
+            m_w[h] = -INFINITY;
+            l_l[h] = 0.f;
 #pragma unroll
-        for (int c = 0; c < CPL / 2; ++c) o[h][c] = make_float2(0.f, 0.f);
-    for (int i = ntw; i < total; ++i) {
-        if (i + kWarpStages - 1 < total) issue(i + kWarpStages - 1);
-        cp_async_commit();
-        cp_async_wait_prev();
-        __syncwarp();
-        const int tile = warp + kAttnWarps * (i - ntw);
-        const int nrows = min(kRows, n - tile * kRows);
-        const uint8_t* stage = ring + (size_t)(i % kWarpStages) * C::sz_stage;
-        for (int r = 0; r < nrows; ++r) {
-            const int jl = tile * kRows + r;
-            const uint8_t* row = stage + (size_t)r * ROWB;
-            float p[GP];
-#pragma unroll
-            for (int h = 0; h < GP; h += 4) {
-                const float4 t = *reinterpret_cast<const float4*>(zp + (size_t)jl * GP + h);
-                p[h] = t.x; p[h + 1] = t.y; p[h + 2] = t.z; p[h + 3] = t.w;
-            }
-            float2 v[CPL / 2];
-            if (loc_tier(rl_s[jl]) != 2) {
-                if (CPL == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
-                    v[0] = bf16x2_to_float2(w.x);
-                    v[CPL / 2 - 1] = bf16x2_to_float2(w.y);
-                } else {
-                    v[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + lane * 4));
-                }
-            } else {
-                const float sc = *reinterpret_cast<const float*>(row + D);
-#pragma unroll
-                for (int h = 0; h < G; ++h) p[h] *= sc;
-                if (CPL == 4) {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
-                    v[0] = e4m3x2_to_float2((uint16_t)(w & 0xFFFF));
-                    v[CPL / 2 - 1] = e4m3x2_to_float2((uint16_t)(w >> 16));
-                } else {
-                    v[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(row + lane * 2));
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int c = 0; c < CPL / 2; ++c)
-                    o[h][c] = __ffma2_rn(make_float2(p[h], p[h]), v[c], o[h][c]);
+            for (int c = 0; c < CPL / 2; ++c) o[h][c] = make_float2(0.f, 0.f);
         }
-        __syncwarp();
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncwarp();
-
-    // combine the warps' partial O (fixed order); each warp's ring is free now
-    {
-        float* ored = reinterpret_cast<float*>(ring);
+    };
+    // merges the four warps' (m, l, O) of group g into this CTA's partial record for g
+    auto flush_segment = [&](int g) {
+        float* cw = comb + (size_t)warp * PS;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float l = l_l[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (lane == h) {
+                cw[h] = m_w[h];
+                cw[8 + h] = l;
+            }
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
             for (int c = 0; c < CPL / 2; ++c)
-                *reinterpret_cast<float2*>(ored + (size_t)h * D + lane * CPL + 2 * c) = o[h][c];
-    }
-    __syncthreads();
-    for (int i = tid; i < G * D; i += NT) {
-        float acc = 0.f;
-        for (int w = 0; w < kAttnWarps; ++w)
-            acc += reinterpret_cast<const float*>(smem + C::off_ring + (size_t)w * C::sz_warp_ring)[i];
-        o_s[i] = acc;
-    }
+                *reinterpret_cast<float2*>(cw + 16 + h * D + lane * CPL + 2 * c) = o[h][c];
+        __syncthreads();
+        float* pout = a.part + ((size_t)blockIdx.x * a.part_segments + (g - g_first)) * PS;
+        for (int i = tid; i < G * D + G; i += NT) {
+            const int h = i < G * D ? i / D : i - G * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, comb[w * PS + h]);
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) {
+                const float mw = comb[w * PS + h];
+                const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                acc += f * (i < G * D ? comb[w * PS + 16 + i] : comb[w * PS + 8 + h]);
+            }
+            if (i < G * D) {
+                pout[16 + i] = acc;
+            } else {
+                pout[h] = M;
+                pout[8 + h] = acc;
+            }
+        }
+        __syncthreads();
+    };
 
-    // ------------------------------------------------------------ cluster merge
-    cluster_sync_all();
-    if (tid < kMaxSplits * 8) {
-        const int r = tid >> 3, h = tid & 7;
-        if (r < S && h < G) {
-            mall[tid] = dsmem_ld_f32(dsmem_addr(smem_u32(m_s + h), r));
-            lall[tid] = dsmem_ld_f32(dsmem_addr(smem_u32(l_s + h), r));
+    int cur_group = -1;
+    for (int item = it0; item < it1; ++item) {
+        const int g = item / IPG, b = g / a.Hkv, kvh = g % a.Hkv;
+        const int j0 = (item % IPG) * IT;
+        const int n = n_s[item - it0];
+        if (g != cur_group) {
+            if (cur_group >= 0) flush_segment(cur_group);
+            else __syncthreads();
+            for (int i = tid; i < G * D; i += NT)
+                q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kvh * G) * D + i]) * a.qscale;
+            __syncthreads();
+            reset_segment();
+            cur_group = g;
+        }
+        const int nt = warp_tiles(n);
+        float* zg = a.zs + (((size_t)b * a.Hkv + kvh) * a.Nmax + j0) * GP;
+        for (int k = 0; k < nt; ++k) {
+            const int tile = warp + kAttnWarps * k;
+            const int jl = tile * kRows + lane;
+            const bool valid = jl < n;
+
+            // ---------------------------------------------------------- K tile
+            issue_next();                       // the V tile of this tile
+            cp_async_commit();
+            const uint32_t tmask = fp8_mask_issue;
+            cp_async_wait_prev();
+            __syncwarp();
+            float z[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) z[h] = -INFINITY;
+            if (valid) {
+                const uint8_t* row = ring + (size_t)(consumed % kWarpStages) * C::sz_stage + (size_t)lane * ROWB;
+                // two independent accumulator pairs per head: (k0, k2) and (k1, k3) of each chunk
+                float2 acc[G], acc2[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) acc[h] = acc2[h] = make_float2(0.f, 0.f);
+                float zscale = 1.0f;
+                if (!((tmask >> lane) & 1u)) {
+#pragma unroll 4
+                    for (int c = 0; c < D / 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
+                        const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+                        const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
+                            const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
+                            acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
+                            acc2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[h]);
+                            acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
+                            acc2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[h]);
+                        }
+                    }
+                } else {
+                    zscale = *reinterpret_cast<const float*>(row + D);
+#pragma unroll 4
+                    for (int c = 0; c < D / 8; ++c) {
+                        const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
+                        const float2 k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
+                        const float2 k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
+                        const float2 k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
+                        const float2 k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
+                            const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
+                            acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
+                            acc2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[h]);
+                            acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
+                            acc2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[h]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) z[h] = ((acc[h].x + acc[h].y) + (acc2[h].x + acc2[h].y)) * zscale;
+            }
+            __syncwarp();
+            ++consumed;
+
+            // ------------------------------ online softmax update (warp-uniform max)
+            float p[GP];
+#pragma unroll
+            for (int h = 0; h < GP; ++h) p[h] = 0.f;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float tm = z[h];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
+                const float m_new = fmaxf(m_w[h], tm);
+                const float sc = (m_w[h] == -INFINITY) ? 0.f : exp2f(m_w[h] - m_new);
+                m_w[h] = m_new;
+                l_l[h] *= sc;
+#pragma unroll
+                for (int c = 0; c < CPL / 2; ++c) o[h][c] = __fmul2_rn(o[h][c], make_float2(sc, sc));
+                if (valid) {
+                    p[h] = exp2f(z[h] - m_new);
+                    l_l[h] += p[h];
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < GP; h += 4)
+                *reinterpret_cast<float4*>(p_s + (size_t)lane * GP + h) = make_float4(p[h], p[h + 1], p[h + 2], p[h + 3]);
+            if (valid) {
+                float zz[GP];
+#pragma unroll
+                for (int h = 0; h < GP; ++h) zz[h] = h < G ? z[h] : 0.f;
+#pragma unroll
+                for (int h = 0; h < GP; h += 4)
+                    *reinterpret_cast<float4*>(zg + (size_t)jl * GP + h) = make_float4(zz[h], zz[h + 1], zz[h + 2], zz[h + 3]);
+            }
+            __syncwarp();
+
+            // ---------------------------------------------------------- V tile
+            issue_next();                       // the next K tile
+            cp_async_commit();
+            cp_async_wait_prev();
+            __syncwarp();
+            {
+                const int nrows = min(kRows, n - tile * kRows);
+                const uint8_t* stage = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
+#pragma unroll 2
+                for (int r = 0; r < nrows; ++r) {
+                    const uint8_t* row = stage + (size_t)r * ROWB;
+                    float pr[GP];
+#pragma unroll
+                    for (int h = 0; h < GP; h += 4) {
+                        const float4 t = *reinterpret_cast<const float4*>(p_s + (size_t)r * GP + h);
+                        pr[h] = t.x; pr[h + 1] = t.y; pr[h + 2] = t.z; pr[h + 3] = t.w;
+                    }
+                    float2 v[CPL / 2];
+                    if (!((tmask >> r) & 1u)) {
+                        if (CPL == 4) {
+                            const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
+                            v[0] = bf16x2_to_float2(w.x);
+                            v[CPL / 2 - 1] = bf16x2_to_float2(w.y);
+                        } else {
+                            v[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + lane * 4));
+                        }
+                    } else {
+                        const float sc = *reinterpret_cast<const float*>(row + D);
+#pragma unroll
+                        for (int h = 0; h < G; ++h) pr[h] *= sc;
+                        if (CPL == 4) {
+                            const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
+                            v[0] = e4m3x2_to_float2((uint16_t)(w & 0xFFFF));
+                            v[CPL / 2 - 1] = e4m3x2_to_float2((uint16_t)(w >> 16));
+                        } else {
+                            v[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(row + lane * 2));
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int c = 0; c < CPL / 2; ++c)
+                            o[h][c] = __ffma2_rn(make_float2(pr[h], pr[h]), v[c], o[h][c]);
+                }
+            }
+            __syncwarp();
+            ++consumed;
         }
     }
-    __syncthreads();
-    if (tid < G) {
-        const int h = tid;
+    flush_segment(cur_group);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Merges a group's partials (one per CTA whose range touches the group, in CTA
+// order) into `out`, and writes the per-position sum over the group's query
+// heads of alpha = 2^(z - M) / L.
+template <int G, int D>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+    using C = AttnCfg<G, D>;
+    constexpr int GP = C::GP, PS = C::PS;
+    extern __shared__ __align__(16) float fsm[];     // f[segment][8]
+    __shared__ float Ms[8], Linv[8];
+    const int g = blockIdx.y, b = g / a.Hkv, kvh = g % a.Hkv;
+    const int R = a.rl_count[b];
+    const int IPG = a.items_per_group, ipc = a.items_per_cta;
+    const int c_lo = (g * IPG) / ipc, c_hi = ((g + 1) * IPG - 1) / ipc;
+    const int ns = c_hi - c_lo + 1;
+    auto rec = [&](int s) {
+        const int c = c_lo + s;
+        const int seg = g - (c * ipc) / IPG;
+        return a.part + ((size_t)c * a.part_segments + seg) * PS;
+    };
+    if (threadIdx.x < G) {
+        const int h = threadIdx.x;
         float M = -INFINITY;
-        for (int r = 0; r < S; ++r) M = fmaxf(M, mall[r * 8 + h]);
-        float Lsum = 0.f;
-        for (int r = 0; r < S; ++r) {
-            const float mr = mall[r * 8 + h];
-            const float e = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
-            f_s[r * 8 + h] = e;
-            Lsum += lall[r * 8 + h] * e;
+        for (int s = 0; s < ns; ++s) M = fmaxf(M, rec(s)[h]);
+        float L = 0.f;
+        for (int s = 0; s < ns; ++s) {
+            const float ms = rec(s)[h];
+            const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+            fsm[s * 8 + h] = f;
+            L += f * rec(s)[8 + h];
         }
-        const float inv = 1.0f / Lsum;
-        for (int r = 0; r < S; ++r) f_s[r * 8 + h] *= inv;
+        const float inv = 1.0f / L;
+        for (int s = 0; s < ns; ++s) fsm[s * 8 + h] *= inv;
+        Ms[h] = M;
+        Linv[h] = inv;
     }
     __syncthreads();
-
-    // alpha sums over the group's query heads, for this CTA's rows
-    {
-        float f_self[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) f_self[h] = f_s[rank * 8 + h];
-        float* gdst = a.g + (((size_t)a.layer * a.B + b) * a.Hkv + kvh) * a.Nmax + j0;
-        for (int jl = tid; jl < n; jl += NT) {
+    if (blockIdx.x == 0) {
+        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+            const int h = idx / D;
             float acc = 0.f;
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc += zp[(size_t)jl * GP + h] * f_self[h];
-            gdst[jl] = acc;
+            for (int s = 0; s < ns; ++s) acc += rec(s)[16 + idx] * fsm[s * 8 + h];
+            a.out[((size_t)b * a.Hq + (size_t)kvh * G) * D + idx] = acc;
         }
     }
-
-    // this CTA's share of the output, reduced over the peers in rank order
-    {
-        const int per = (G * D + S - 1) / S;
-        const int i0 = rank * per, i1 = min(G * D, i0 + per);
-        const uint32_t ao = smem_u32(o_s);
-        for (int i = i0 + tid; i < i1; i += NT) {
-            const int h = i / D, c = i % D;
-            float v[kMaxSplits];
+    const float* zg = a.zs + ((size_t)b * a.Hkv + kvh) * a.Nmax * GP;
+    float* gdst = a.g + (((size_t)a.layer * a.B + b) * a.Hkv + kvh) * a.Nmax;
+    const int j_end = min(R, (int)(blockIdx.x + 1) * kCombineRows);
+    for (int j = blockIdx.x * kCombineRows + threadIdx.x; j < j_end; j += blockDim.x) {
+        float zz[GP];
 #pragma unroll
-            for (int r = 0; r < kMaxSplits; ++r)
-                v[r] = (r < S) ? dsmem_ld_f32(dsmem_addr(ao + 4u * i, r)) : 0.f;
-            float acc = 0.f;
-#pragma unroll
-            for (int r = 0; r < kMaxSplits; ++r)
-                if (r < S) acc += v[r] * f_s[r * 8 + h];
-            a.out[((size_t)b * a.Hq + (size_t)kvh * G + h) * D + c] = acc;
+        for (int h = 0; h < GP; h += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(zg + (size_t)j * GP + h);
+            zz[h] = t.x; zz[h + 1] = t.y; zz[h + 2] = t.z; zz[h + 3] = t.w;
         }
+        float acc = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc += exp2f(zz[h] - Ms[h]) * Linv[h];
+        gdst[j] = acc;
     }
-    cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ dispatch
 template <int G, int D>
 static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
-    const size_t smem = AttnCfg<G, D>::smem(a.chunk);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.splits, a.Hkv, a.B);
-    cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<G, D>, a);
+    using C = AttnCfg<G, D>;
+    const size_t smem = C::smem(a.items_per_cta * a.item_rows);
+    attn_kernel<G, D><<<a.grid, kAttnWarps * 32, smem, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int rmax_blocks = (a.items_per_group * a.item_rows + kCombineRows - 1) / kCombineRows;
+    dim3 grid(rmax_blocks, a.B * a.Hkv);
+    const int max_segs = (a.items_per_group + a.items_per_cta - 1) / a.items_per_cta + 1;
+    attn_combine_kernel<G, D><<<grid, 256, (size_t)max_segs * 8 * 4, st>>>(a);
+    return cudaGetLastError();
 }
 
 template <int G, int D>
 static cudaError_t prepare_gd(size_t smem) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<G, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(attn_kernel<G, D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cudaFuncSetAttribute(attn_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
 template <int G, int D>
-static bool cluster_fits_gd(size_t smem, int s) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(s, 1, 1);
-    cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = s;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<G, D>, &cfg) == cudaSuccess && n > 0) return true;
-    (void)cudaGetLastError();
-    return false;
+static size_t smem_gd(int rl_rows) {
+    return AttnCfg<G, D>::smem(rl_rows);
+}
+
+template <int G, int D>
+static int resident_gd(size_t smem) {
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_kernel<G, D>, kAttnWarps * 32, smem) != cudaSuccess ||
+        cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return per_sm * sms;
+}
+
+template <int G, int D>
+static cudaError_t ensure_smem_gd(size_t smem) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_kernel<G, D>);
+    if (e != cudaSuccess) return e;
+    if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
+    return prepare_gd<G, D>(smem);
 }
 
 #define TKV_DISPATCH_G(D, FN, ...)                      \
@@ -463,14 +541,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st) {
     return cudaErrorInvalidValue;
 }
 
-template <int G, int D>
-static size_t smem_gd(int chunk) {
-    return AttnCfg<G, D>::smem(chunk);
-}
-
-size_t attention_smem_bytes(int G, int d, int chunk) {
-    if (d == 128) { TKV_DISPATCH_G(128, smem_gd, chunk) }
-    if (d == 64) { TKV_DISPATCH_G(64, smem_gd, chunk) }
+size_t attention_smem_bytes(int G, int d, int rl_rows) {
+    if (d == 128) { TKV_DISPATCH_G(128, smem_gd, rl_rows) }
+    if (d == 64) { TKV_DISPATCH_G(64, smem_gd, rl_rows) }
     return 0;
 }
 
@@ -480,13 +553,10 @@ cudaError_t attention_prepare(int G, int d, size_t smem) {
     return cudaErrorInvalidValue;
 }
 
-template <int G, int D>
-static cudaError_t ensure_smem_gd(size_t smem) {
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_kernel<G, D>);
-    if (e != cudaSuccess) return e;
-    if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
-    return prepare_gd<G, D>(smem);
+int attention_resident_ctas(int G, int d, size_t smem) {
+    if (d == 128) { TKV_DISPATCH_G(128, resident_gd, smem) }
+    if (d == 64) { TKV_DISPATCH_G(64, resident_gd, smem) }
+    return 0;
 }
 
 cudaError_t attention_ensure_smem(int G, int d, size_t smem) {
@@ -495,10 +565,37 @@ cudaError_t attention_ensure_smem(int G, int d, size_t smem) {
     return cudaErrorInvalidValue;
 }
 
-bool attention_cluster_fits(int G, int d, size_t smem, int splits) {
-    if (d == 128) { TKV_DISPATCH_G(128, cluster_fits_gd, smem, splits) }
-    if (d == 64) { TKV_DISPATCH_G(64, cluster_fits_gd, smem, splits) }
-    return false;
+AttnPlan attention_plan(int G, int d, int B, int Hkv, int rmax, int resident) {
+    AttnPlan p{};
+    const int groups = B * Hkv;
+    rmax = std::max(rmax, 1);
+    resident = std::max(resident, 1);
+    // 256-row items, or 128-row items when that is needed to give every resident CTA work
+    p.item_rows = (groups * ((rmax + 255) / 256) >= resident) ? 256 : 128;
+    p.items_per_group = (rmax + p.item_rows - 1) / p.item_rows;
+    const int total = groups * p.items_per_group;
+    p.grid = std::min(total, resident);
+    p.items_per_cta = (total + p.grid - 1) / p.grid;
+    const int max_items = kMaxWindowRows / p.item_rows;
+    if (p.items_per_cta > max_items) {
+        p.items_per_cta = max_items;
+        p.grid = (total + max_items - 1) / max_items;
+    }
+    p.part_segments = (p.items_per_cta + p.items_per_group - 1) / p.items_per_group + 1;
+    p.smem = attention_smem_bytes(G, d, p.items_per_cta * p.item_rows);
+    return p;
+}
+
+size_t attention_part_floats(int G, int d, int B, int Hkv, int Nmax, int resident) {
+    // grid * part_segments records: grid <= max(resident, items / 32), part_segments <= items_per_cta + 1
+    const size_t items = (size_t)B * Hkv * ((Nmax + 127) / 128);
+    const size_t grid = std::max<size_t>((size_t)resident, items / 32 + 1);
+    return (items + 2 * grid + 64) * (16 + (size_t)G * d);
+}
+
+size_t attention_zs_floats(int G, int B, int Hkv, int Nmax) {
+    const int GP = (G <= 4) ? 4 : 8;
+    return (size_t)B * Hkv * Nmax * GP;
 }
 
 // ---------------------------------------------------------------- score fold

@@ -16,6 +16,7 @@
 // size fits; that first call should therefore come before any stream capture.
 // Every call shares the arrays and leaves its contents in them; calls that
 // overlap on the GPU (for example on two streams) race on them.
+#include <cmath>
 #include <mutex>
 
 #include "../../include/tkv.h"
@@ -25,11 +26,18 @@ using namespace tkv;
 
 namespace {
 
-constexpr size_t kMaxAlphaFloats = size_t(1) << 21;   // L*B*Hkv*R  <= 2,097,152  (8 MiB)
-constexpr size_t kMaxTable = size_t(1) << 18;         // B*R        <= 262,144    (1 MiB)
+constexpr size_t kMaxAlphaFloats = size_t(1) << 20;   // L*B*Hkv*R  <= 1,048,576  (4 MiB)
+constexpr size_t kMaxGroupRows = size_t(1) << 17;     // B*Hkv*R    <= 131,072
+constexpr size_t kMaxTable = size_t(1) << 17;         // B*R        <= 131,072    (0.5 MiB)
 constexpr int kMaxBatch = 256;
+constexpr size_t kMaxZsFloats = kMaxGroupRows * 8;    // logits, 8 per row      (4 MiB)
+// softmax partials: (items + 2 * CTAs + 64) records of (16 + 8*128) floats, bounded for
+// B*Hkv*R <= 131,072 and up to 2 * 2048 CTAs
+constexpr size_t kMaxPartFloats = (kMaxGroupRows / 128 + 2048 + 4096 + 64) * (16 + 8 * 128);   // ~29 MiB
 
 static __device__ __align__(256) float g_alpha_scratch[kMaxAlphaFloats];
+static __device__ __align__(256) float g_zs_scratch[kMaxZsFloats];
+static __device__ __align__(256) float g_part_scratch[kMaxPartFloats];
 static __device__ __align__(256) uint32_t g_index_scratch[kMaxTable];
 static __device__ __align__(256) int32_t g_count_scratch[kMaxBatch];
 static __device__ __align__(256) int32_t g_status_scratch[1];
@@ -37,6 +45,8 @@ static __device__ __align__(256) int32_t g_status_scratch[1];
 struct DevScratch {
     bool ready = false;
     float* alpha = nullptr;
+    float* zs = nullptr;
+    float* part = nullptr;
     uint32_t* index = nullptr;
     int32_t* count = nullptr;
     int32_t* status = nullptr;
@@ -60,6 +70,8 @@ tkv_status setup(int dev, DevScratch** out) {
     DevScratch& s = g_dev[dev];
     if (!s.ready) {
         if (cudaGetSymbolAddress((void**)&s.alpha, g_alpha_scratch) != cudaSuccess ||
+            cudaGetSymbolAddress((void**)&s.zs, g_zs_scratch) != cudaSuccess ||
+            cudaGetSymbolAddress((void**)&s.part, g_part_scratch) != cudaSuccess ||
             cudaGetSymbolAddress((void**)&s.index, g_index_scratch) != cudaSuccess ||
             cudaGetSymbolAddress((void**)&s.count, g_count_scratch) != cudaSuccess ||
             cudaGetSymbolAddress((void**)&s.status, g_status_scratch) != cudaSuccess) {
@@ -84,9 +96,10 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
     if (L < 1 || B < 1 || Hkv < 1 || Hq < 1 || R < 1 || Hq % Hkv || Hq / Hkv > 8 || (d != 64 && d != 128))
         return TKV_EINVAL;
     // size limits of the fixed scratch
-    if (B > kMaxBatch || (size_t)B * R > kMaxTable ||
+    if (B > kMaxBatch || (size_t)B * R > kMaxTable || (size_t)B * Hkv * R > kMaxGroupRows ||
         (size_t)L * B * Hkv * R > kMaxAlphaFloats)
         return TKV_ECAPACITY;
+
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         (void)cudaGetLastError();
@@ -98,21 +111,16 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
     cudaStream_t st = (cudaStream_t)stream;
     const int G = Hq / Hkv;
 
-    // same work split as the context path: S = clamp(ceil(R / 256), 1, largest cluster that fits)
-    int S = std::min(kMaxSplits, std::max(1, (R + 255) / 256));
-    int chunk = 0;
-    size_t smem = 0;
-    for (; S >= 1; --S) {
-        chunk = ((R + S - 1) / S + kRows - 1) / kRows * kRows;
-        smem = attention_smem_bytes(G, d, chunk);
-        if (smem > 227 * 1024) return TKV_ECAPACITY;
-        if (attention_ensure_smem(G, d, smem) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return TKV_ECUDA;
-        }
-        if (attention_cluster_fits(G, d, smem, S)) break;
+    // same launch plan as the context path
+    const size_t smem_max = attention_smem_bytes(G, d, 4096);
+    if (attention_ensure_smem(G, d, smem_max) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TKV_ECUDA;
     }
-    if (S < 1) return TKV_ECUDA;
+    const int resident = attention_resident_ctas(G, d, smem_max);
+    if (resident < 1) return TKV_ECUDA;
+    const AttnPlan plan = attention_plan(G, d, B, Hkv, R, resident);
+    if (attention_part_floats(G, d, B, Hkv, R, resident) > kMaxPartFloats) return TKV_ECAPACITY;
 
     noalloc_fill_kernel<<<(B * R + 255) / 256, 256, 0, st>>>(sc->index, sc->count, sc->status, B, R);
     if (cudaGetLastError() != cudaSuccess) return TKV_ECUDA;
@@ -124,10 +132,16 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
     a.rl_loc = sc->index;
     a.rl_count = sc->count;
     a.g = sc->alpha;
+    a.part = sc->part;
+    a.zs = sc->zs;
     a.err = sc->status;
     a.L = L; a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.d = d;
     a.Nmax = R; a.S0 = R; a.S1 = 0; a.S2 = 0;
-    a.splits = S; a.chunk = chunk;
+    a.item_rows = plan.item_rows;
+    a.items_per_group = plan.items_per_group;
+    a.items_per_cta = plan.items_per_cta;
+    a.grid = plan.grid;
+    a.part_segments = plan.part_segments;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)d));
     for (int l = 0; l < L; ++l) {
         a.layer = l;

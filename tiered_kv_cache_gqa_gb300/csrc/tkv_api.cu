@@ -39,6 +39,7 @@ struct tkv_ctx {
     uint32_t* rl_loc = nullptr;
     int32_t *rl_pos = nullptr, *rl_count = nullptr;
     float* g = nullptr;
+    float *part = nullptr, *zs = nullptr;    // attention scratch: item partials, logits
     int32_t *t0_free = nullptr, *t0_top = nullptr;
     int4 *moves_now = nullptr, *moves_delta = nullptr;
     RetierOut* outp = nullptr;
@@ -66,7 +67,7 @@ struct tkv_ctx {
     std::vector<char> prefetched;
     int delta_max = 0;                 // pending delta moves (max over sequences), 0 = none
 
-    int splits_max = 1;
+    int resident = 1;                  // attention CTAs resident on the device at once
     int last_splits = 0;
 
     // timing (tkv_profile_begin / tkv_profile_end): kinds 0 attention, 1 T1 copy, 2 delta
@@ -153,7 +154,7 @@ void free_all(tkv_ctx* c) {
     cudaFree(c->tier); cudaFree(c->new_tier); cudaFree(c->forced);
     cudaFree(c->slot); cudaFree(c->new_slot); cudaFree(c->free_scratch);
     cudaFree(c->s); cudaFree(c->rl_loc); cudaFree(c->rl_pos); cudaFree(c->rl_count);
-    cudaFree(c->g); cudaFree(c->t0_free); cudaFree(c->t0_top);
+    cudaFree(c->g); cudaFree(c->part); cudaFree(c->zs); cudaFree(c->t0_free); cudaFree(c->t0_top);
     cudaFree(c->moves_now); cudaFree(c->moves_delta); cudaFree(c->outp); cudaFree(c->params);
     cudaFree(c->err);
     cudaFreeHost(c->h1); cudaFreeHost(c->h2m); cudaFreeHost(c->h_outp); cudaFreeHost(c->h_params);
@@ -437,6 +438,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     A(dalloc(ctx, &ctx->rl_pos, B * Nmax));
     A(dalloc(ctx, &ctx->rl_count, B));
     A(dalloc(ctx, &ctx->g, L * B * Hkv * Nmax));
+    A(dalloc(ctx, &ctx->zs, attention_zs_floats(G, (int)B, (int)Hkv, (int)Nmax)));
     A(dalloc(ctx, &ctx->t0_free, B * S0));
     A(dalloc(ctx, &ctx->t0_top, B));
     A(dalloc(ctx, &ctx->moves_now, B * Nmax));
@@ -489,23 +491,18 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
         return bail(TKV_ECUDA);
     }
 
-    // kernel set-up: the largest cluster size whose largest launch fits.  A
-    // launch with R retained rows uses S = clamp(ceil(R / 256), 1, Smax) CTAs
-    // per cluster and runs of ceil(R / S) rows rounded up to 32, so a run is at
-    // most max(256, ceil(Nmax / Smax)) rows.
-    ctx->splits_max = 0;
-    for (int S = kMaxSplits; S >= 1; S >>= 1) {
-        const int cap = std::max(256, (int)((Nmax + S - 1) / S));
-        const int chunk = (cap + kRows - 1) / kRows * kRows;
-        const size_t smem = attention_smem_bytes(G, ctx->d, chunk);
-        if (smem > 227 * 1024) continue;
+    // kernel set-up: the largest attention launch stages 4096 retained rows per CTA
+    {
+        const size_t smem = attention_smem_bytes(G, ctx->d, 4096);
         if (attention_prepare(G, ctx->d, smem) != cudaSuccess) return bail(TKV_ECUDA);
-        if (attention_cluster_fits(G, ctx->d, smem, S)) {
-            ctx->splits_max = S;
-            break;
+        ctx->resident = attention_resident_ctas(G, ctx->d, smem);
+        if (ctx->resident < 1) return bail(TKV_ECUDA);
+        if (dalloc(ctx, &ctx->part, attention_part_floats(G, ctx->d, ctx->B, ctx->Hkv, ctx->Nmax, ctx->resident)) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return bail(TKV_ENOMEM);
         }
     }
-    if (ctx->splits_max < 1) return bail(TKV_EINVAL);
     if (retier_prepare(retier_smem_bytes(ctx->S0, ctx->S1, ctx->S2)) != cudaSuccess) return bail(TKV_ECUDA);
 
     for (int t = 0; t < 4; ++t) ctx->count[t].assign(B, 0);
@@ -583,8 +580,7 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
 
     int rmax = 0;
     for (int b = 0; b < ctx->B; ++b) rmax = std::max(rmax, ctx->R[b]);
-    int S = std::min(ctx->splits_max, std::max(1, (rmax + 255) / 256));
-    int chunk = ((rmax + S - 1) / S + kRows - 1) / kRows * kRows;
+    const AttnPlan plan = attention_plan(ctx->G, ctx->d, ctx->B, ctx->Hkv, rmax, ctx->resident);
     AttnArgs a{};
     a.q = (const __nv_bfloat16*)q;
     a.out = out;
@@ -594,14 +590,20 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
     a.rl_loc = ctx->rl_loc;
     a.rl_count = ctx->rl_count;
     a.g = ctx->g;
+    a.part = ctx->part;
+    a.zs = ctx->zs;
     a.err = ctx->err;
     a.layer = layer; a.L = ctx->L; a.B = ctx->B; a.Hq = ctx->Hq; a.Hkv = ctx->Hkv; a.d = ctx->d;
     a.Nmax = ctx->Nmax; a.S0 = ctx->S0; a.S1 = ctx->S1; a.S2 = ctx->S2;
-    a.splits = S; a.chunk = chunk;
+    a.item_rows = plan.item_rows;
+    a.items_per_group = plan.items_per_group;
+    a.items_per_cta = plan.items_per_cta;
+    a.grid = plan.grid;
+    a.part_segments = plan.part_segments;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)ctx->d));
     const bool timed = prof_open(ctx, 0, ctx->compute);
     CK(launch_attention(a, ctx->compute));
-    ctx->launches++;
+    ctx->launches += 2;
     if (timed) {
         double bytes = (double)ctx->B * ctx->Hq * ctx->d * (2 + 4);
         for (int b = 0; b < ctx->B; ++b)
@@ -610,7 +612,7 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
         prof_close(ctx, 0, ctx->compute, bytes);
     }
     CK(cudaEventRecord(ctx->ev_attn[slotr], ctx->compute));
-    ctx->last_splits = S;
+    ctx->last_splits = plan.grid;
     ctx->decoded++;
     if (ctx->decoded == ctx->L) {
         const float inv = (float)(1.0 / ((double)ctx->L * (double)ctx->Hq));

@@ -122,17 +122,34 @@ struct AttnArgs {
     const uint8_t* t2;           // T2 pool (all layers)
     const uint32_t* rl_loc;      // [B][Nmax]
     const int32_t* rl_count;     // [B]
-    float* g;                    // [L][B][Hkv][Nmax]
+    float* g;                    // [L][B][Hkv][Nmax]  per-position alpha sums (written by the combine)
+    float* part;                 // [grid][part_segments][16 + G*d] softmax partials per (CTA, group) (scratch)
+    float* zs;                   // [B][Hkv][Nmax][GP] logits, log2-scaled (scratch)
     int32_t* err;                // status word (unused by kernels without device waits)
     int layer, L, B, Hq, Hkv, d, Nmax, S0, S1, S2;
-    int splits, chunk;           // CTAs per (b, kv head) and retained rows per CTA
+    int items_per_group;         // ceil(max_b R_b / item_rows)
+    int item_rows;               // rows per item, a multiple of 128
+    int items_per_cta;           // contiguous items per CTA
+    int grid;                    // CTAs of the main kernel
+    int part_segments;           // partial records per CTA (groups a CTA's range can touch)
     float qscale;                // log2(e) / sqrt(d)
 };
 
+// Launch geometry shared by the context path and the allocation-free path.
+struct AttnPlan {
+    int item_rows, items_per_group, items_per_cta, grid, part_segments;
+    size_t smem;
+};
+// Plans a launch for B sequences x Hkv heads with at most rmax retained rows.
+// `resident` = CTAs of the main kernel that fit on the device at once.
+AttnPlan attention_plan(int G, int d, int B, int Hkv, int rmax, int resident);
+size_t attention_part_floats(int G, int d, int B, int Hkv, int Nmax, int resident);   // scratch sizes
+size_t attention_zs_floats(int G, int B, int Hkv, int Nmax);
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
-size_t attention_smem_bytes(int G, int d, int chunk);
+size_t attention_smem_bytes(int G, int d, int rl_rows);
 cudaError_t attention_prepare(int G, int d, size_t smem);
-bool attention_cluster_fits(int G, int d, size_t smem, int splits);
+int attention_resident_ctas(int G, int d, size_t smem);                  // CTAs per device
 cudaError_t attention_ensure_smem(int G, int d, size_t smem);   // raises the cap, never lowers it
 
 cudaError_t launch_fold(const float* g, const int32_t* rl_pos, const int32_t* rl_count, float* s,
