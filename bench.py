@@ -53,7 +53,7 @@ def parse():
     p.add_argument("--t3", type=float, default=None, help="eviction ratio")
     p.add_argument("--layers", type=int, default=None,
                    help="override the layer count (small captures for ncu; per-launch size unchanged)")
-    p.add_argument("--t1", choices=["ce", "sm", "split"], default="ce",
+    p.add_argument("--t1", choices=["ce", "sm", "split", "multi"], default="ce",
                    help="T1 transport: copy engine, SM copy kernel, or both")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -226,7 +226,8 @@ def run_gpu(args, rank, world):
     wl = wl.with_(seed=wl.seed + 1000 * rank)
     L, B, Hq, Hkv, d = wl.num_layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     stream = torch.cuda.current_stream()
-    t1_mode = {"ce": tkv.TKV_T1_COPY_ENGINE, "sm": tkv.TKV_T1_SM_COPY, "split": tkv.TKV_T1_SPLIT}[args.t1]
+    t1_mode = {"ce": tkv.TKV_T1_COPY_ENGINE, "sm": tkv.TKV_T1_SM_COPY, "split": tkv.TKV_T1_SPLIT,
+               "multi": tkv.TKV_T1_MULTI_CE}[args.t1]
     ctx = tkv.TieredKV.for_workload(wl, device=dev, t1_transport=t1_mode)
     gen = synth.Generator(wl, device="cuda")
     for l in range(L):

@@ -68,8 +68,10 @@ typedef struct tkv_ctx tkv_ctx;
  *                       the pinned host rows directly (zero-copy) and store
  *                       them to staging
  *   TKV_T1_SPLIT        half the rows by the copy engine, half by the copy
- *                       kernel on a second stream, concurrently */
-enum { TKV_T1_COPY_ENGINE = 0, TKV_T1_SM_COPY = 1, TKV_T1_SPLIT = 2 };
+ *                       kernel on a second stream, concurrently
+ *   TKV_T1_MULTI_CE     the rows split four ways over four copy streams, so
+ *                       that several copy engines run at once */
+enum { TKV_T1_COPY_ENGINE = 0, TKV_T1_SM_COPY = 1, TKV_T1_SPLIT = 2, TKV_T1_MULTI_CE = 3 };
 
 typedef struct {
     int32_t num_layers;       /* L >= 1 */

@@ -237,7 +237,7 @@ def test_t1_transports_are_bitwise_identical():
     wl = synth.Workload("t1x", 3, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
                         window=16, ratios=(0.3, 0.6, 0.05, 0.05), seed=8)
     outs = []
-    for mode in (tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T1_SM_COPY, tkv.TKV_T1_SPLIT):
+    for mode in (tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T1_SM_COPY, tkv.TKV_T1_SPLIT, tkv.TKV_T1_MULTI_CE):
         gen = synth.Generator(wl)
         ctx = tkv.TieredKV.for_workload(wl, t1_transport=mode)
         prefill_both(ctx, None, gen)

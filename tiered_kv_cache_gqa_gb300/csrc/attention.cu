@@ -59,7 +59,7 @@ struct AttnCfg {
     static constexpr size_t off_ring = 0;
     static constexpr size_t off_q = kAttnWarps * sz_warp_ring;
     static constexpr size_t off_p = off_q + (size_t)G * D * 4;
-    static constexpr size_t off_comb = off_p + (size_t)kAttnWarps * kRows * GP * 4;
+    static constexpr size_t off_comb = off_p + (size_t)kAttnWarps * kRows * 2 * GP * 4;   // p as (p, p) pairs
     static constexpr size_t off_n = off_comb + (size_t)kAttnWarps * PS * 4;   // rows of each item
     static constexpr size_t off_rl = off_n + (size_t)(kMaxWindowRows / 128) * 4;
 
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     if (it0 >= it1) return;
     const int g_first = it0 / IPG;
     uint8_t* ring = smem + C::off_ring + (size_t)warp * C::sz_warp_ring;
-    float* p_s = reinterpret_cast<float*>(smem + C::off_p) + (size_t)warp * kRows * GP;
+    float* p_s = reinterpret_cast<float*>(smem + C::off_p) + (size_t)warp * kRows * 2 * GP;
 
     // rows of every item of this CTA, and their retained-list slices
     for (int item = it0 + tid; item < it1; item += NT) {
@@ -124,60 +124,56 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     settle();
     const uint8_t* k0v0 = reinterpret_cast<const uint8_t*>(a.k0v0);
     const uint8_t* stg = reinterpret_cast<const uint8_t*>(a.stage);
-    // the lane's row of the tile being issued: K address, V address, byte count
-    const uint8_t* row_v = nullptr;
+    const uint8_t* row_v = nullptr;    // the lane's V row of the tile whose K was issued last
     int row_bytes = 0;
     uint32_t fp8_mask_issue = 0;       // T2 rows of the tile last issued as K
+    // Copies the next tile of this warp's sequence: 16 lanes per 256-byte row, 16 bytes
+    // a lane; a row's source pointer travels by shuffle with its kind in the low bits
+    // (bit 0: T2 record of D + 16 bytes, bit 1: no row).
     auto issue_next = [&]() {
         if (ci_item >= it1) return;
         const int item = ci_item, kv = ci_kv;
         const int n = n_s[item - it0];
         const int tile = warp + kAttnWarps * ci_k;
         const int jl = tile * kRows + lane;
+        const uint8_t* src = nullptr;
         if (kv == 0) {
             const int g = item / IPG, b = g / a.Hkv, kvh = g % a.Hkv;
-            const uint8_t* row_k = nullptr;
             row_bytes = 0;
             bool fp8 = false;
             if (jl < n) {
                 const uint32_t loc = rl_s[(size_t)(item - it0) * IT + jl];
-                const int tier = loc_tier(loc);
-                const size_t slot = (size_t)loc_slot(loc);
+                const int tier = loc_tier(loc), slot = loc_slot(loc);
                 if (tier == 0) {
-                    row_k = k0v0 + row_index(a.layer, 0, b, kvh, (int)slot, a.B, a.Hkv, a.S0) * (2 * D);
-                    row_v = k0v0 + row_index(a.layer, 1, b, kvh, (int)slot, a.B, a.Hkv, a.S0) * (2 * D);
+                    src = k0v0 + row_index(a.layer, 0, b, kvh, slot, a.B, a.Hkv, a.S0) * (2 * D);
+                    row_v = k0v0 + row_index(a.layer, 1, b, kvh, slot, a.B, a.Hkv, a.S0) * (2 * D);
                     row_bytes = 2 * D;
                 } else if (tier == 1) {
-                    row_k = stg + row_index(0, 0, b, kvh, (int)slot, a.B, a.Hkv, a.S1) * (2 * D);
-                    row_v = stg + row_index(0, 1, b, kvh, (int)slot, a.B, a.Hkv, a.S1) * (2 * D);
+                    src = stg + row_index(0, 0, b, kvh, slot, a.B, a.Hkv, a.S1) * (2 * D);
+                    row_v = stg + row_index(0, 1, b, kvh, slot, a.B, a.Hkv, a.S1) * (2 * D);
                     row_bytes = 2 * D;
                 } else {
-                    row_k = a.t2 + row_index(a.layer, 0, b, kvh, (int)slot, a.B, a.Hkv, a.S2) * (D + 16);
-                    row_v = a.t2 + row_index(a.layer, 1, b, kvh, (int)slot, a.B, a.Hkv, a.S2) * (D + 16);
+                    src = a.t2 + row_index(a.layer, 0, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
+                    row_v = a.t2 + row_index(a.layer, 1, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
                     row_bytes = D + 16;
                     fp8 = true;
                 }
             }
             fp8_mask_issue = __ballot_sync(0xffffffffu, fp8);
-            const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * C::sz_stage);
-            const int col = lane & 15, half = lane >> 4;
-#pragma unroll 4
-            for (int rr = 0; rr < kRows / 2; ++rr) {
-                const int r = 2 * rr + half;
-                const uint8_t* src = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)row_k, r);
-                const int nb = __shfl_sync(0xffffffffu, row_bytes, r);
-                if (col * 16 < nb) cp_async16(dst0 + r * ROWB + col * 16, src + col * 16);
-            }
         } else {
-            const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * C::sz_stage);
-            const int col = lane & 15, half = lane >> 4;
+            src = row_v;
+        }
+        const unsigned long long tagged = (unsigned long long)src | (row_bytes == D + 16 ? 1ull : 0ull) |
+                                          (row_bytes ? 0ull : 2ull);
+        const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * C::sz_stage);
+        const int col = lane & 15, half = lane >> 4;
 #pragma unroll 4
-            for (int rr = 0; rr < kRows / 2; ++rr) {
-                const int r = 2 * rr + half;
-                const uint8_t* src = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)row_v, r);
-                const int nb = __shfl_sync(0xffffffffu, row_bytes, r);
-                if (col * 16 < nb) cp_async16(dst0 + r * ROWB + col * 16, src + col * 16);
-            }
+        for (int rr = 0; rr < kRows / 2; ++rr) {
+            const int r = 2 * rr + half;
+            const unsigned long long t = __shfl_sync(0xffffffffu, tagged, r);
+            const uint8_t* rsrc = (const uint8_t*)(t & ~15ull);
+            const int nb = (t & 2ull) ? 0 : ((t & 1ull) ? D + 16 : 2 * D);
+            if (col * 16 < nb) cp_async16(dst0 + r * ROWB + col * 16, rsrc + col * 16);
         }
         ++issued;
         if (ci_kv == 0) {
@@ -288,7 +284,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                 for (int h = 0; h < G; ++h) acc[h] = acc2[h] = make_float2(0.f, 0.f);
                 float zscale = 1.0f;
                 if (!((tmask >> lane) & 1u)) {
-#pragma unroll 4
+#pragma unroll
                     for (int c = 0; c < D / 8; ++c) {
                         const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
                         const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
@@ -350,8 +346,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                 }
             }
 #pragma unroll
-            for (int h = 0; h < GP; h += 4)
-                *reinterpret_cast<float4*>(p_s + (size_t)lane * GP + h) = make_float4(p[h], p[h + 1], p[h + 2], p[h + 3]);
+            for (int h = 0; h < GP; h += 2)
+                *reinterpret_cast<float4*>(p_s + (size_t)lane * 2 * GP + 2 * h) = make_float4(p[h], p[h], p[h + 1], p[h + 1]);
             if (valid) {
                 float zz[GP];
 #pragma unroll
@@ -370,17 +366,18 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
             {
                 const int nrows = min(kRows, n - tile * kRows);
                 const uint8_t* stage = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
-#pragma unroll 2
-                for (int r = 0; r < nrows; ++r) {
+                // o[h] += p[h] * v for one row; p read as (p, p) pairs
+                auto pv_row = [&](int r, bool fp8) {
                     const uint8_t* row = stage + (size_t)r * ROWB;
-                    float pr[GP];
+                    float2 pp[G];
 #pragma unroll
-                    for (int h = 0; h < GP; h += 4) {
-                        const float4 t = *reinterpret_cast<const float4*>(p_s + (size_t)r * GP + h);
-                        pr[h] = t.x; pr[h + 1] = t.y; pr[h + 2] = t.z; pr[h + 3] = t.w;
+                    for (int h = 0; h < G; h += 2) {
+                        const float4 t = *reinterpret_cast<const float4*>(p_s + (size_t)r * 2 * GP + 2 * h);
+                        pp[h] = make_float2(t.x, t.y);
+                        if (h + 1 < G) pp[h + 1] = make_float2(t.z, t.w);
                     }
                     float2 v[CPL / 2];
-                    if (!((tmask >> r) & 1u)) {
+                    if (!fp8) {
                         if (CPL == 4) {
                             const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
                             v[0] = bf16x2_to_float2(w.x);
@@ -391,7 +388,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                     } else {
                         const float sc = *reinterpret_cast<const float*>(row + D);
 #pragma unroll
-                        for (int h = 0; h < G; ++h) pr[h] *= sc;
+                        for (int h = 0; h < G; ++h) pp[h] = __fmul2_rn(pp[h], make_float2(sc, sc));
                         if (CPL == 4) {
                             const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
                             v[0] = e4m3x2_to_float2((uint16_t)(w & 0xFFFF));
@@ -403,8 +400,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
 #pragma unroll
                     for (int h = 0; h < G; ++h)
 #pragma unroll
-                        for (int c = 0; c < CPL / 2; ++c)
-                            o[h][c] = __ffma2_rn(make_float2(pr[h], pr[h]), v[c], o[h][c]);
+                        for (int c = 0; c < CPL / 2; ++c) o[h][c] = __ffma2_rn(pp[h], v[c], o[h][c]);
+                };
+                if (nrows == kRows && tmask == 0u) {
+#pragma unroll
+                    for (int r = 0; r < kRows; ++r) pv_row(r, false);
+                } else {
+                    for (int r = 0; r < nrows; ++r) pv_row(r, (tmask >> r) & 1u);
                 }
             }
             __syncwarp();

@@ -28,6 +28,9 @@ struct tkv_ctx {
     cudaStream_t compute = nullptr, copy = nullptr, copy2 = nullptr;
     bool own_compute = false, own_copy = false;
     cudaEvent_t ev_split = nullptr;
+    static constexpr int kCopyLanes = 4;                  // streams of the multi-engine T1 transport
+    cudaStream_t copyx[kCopyLanes - 1] = {nullptr, nullptr, nullptr};
+    cudaEvent_t ev_join[kCopyLanes - 1] = {nullptr, nullptr, nullptr};
 
     // device
     __nv_bfloat16* k0v0 = nullptr;
@@ -170,6 +173,10 @@ void free_all(tkv_ctx* c) {
     if (c->own_copy && c->copy) cudaStreamDestroy(c->copy);
     if (c->copy2) cudaStreamDestroy(c->copy2);
     if (c->ev_split) cudaEventDestroy(c->ev_split);
+    for (int i = 0; i < tkv_ctx::kCopyLanes - 1; ++i) {
+        if (c->copyx[i]) cudaStreamDestroy(c->copyx[i]);
+        if (c->ev_join[i]) cudaEventDestroy(c->ev_join[i]);
+    }
     (void)cudaGetLastError();
 }
 
@@ -316,9 +323,33 @@ tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
         const size_t width = (size_t)ctx->hw1 * ctx->d * sizeof(__nv_bfloat16);
         const int height = 2 * ctx->B * ctx->Hkv;
         const int mode = ctx->cfg.t1_transport;
+        const bool timed = prof_open(ctx, 1, ctx->copy);
+        if (mode == TKV_T1_MULTI_CE) {
+            // rows split over the copy stream and kCopyLanes - 1 helper streams
+            const int parts = tkv_ctx::kCopyLanes;
+            for (int k = 1; k < parts; ++k) {
+                const int r0 = height * k / parts, r1 = height * (k + 1) / parts;
+                if (r1 <= r0) continue;
+                cudaStream_t hs = ctx->copyx[k - 1];
+                CK(cudaStreamWaitEvent(hs, ctx->ev_attn[slotr], 0));
+                CK(cudaStreamWaitEvent(hs, ctx->ev_retier, 0));
+                CK(cudaMemcpy2DAsync((uint8_t*)dst + (size_t)r0 * pitch, pitch, (const uint8_t*)src + (size_t)r0 * pitch,
+                                     pitch, width, r1 - r0, cudaMemcpyHostToDevice, hs));
+                CK(cudaEventRecord(ctx->ev_join[k - 1], hs));
+            }
+            const int r1 = height / parts;
+            if (r1 > 0)
+                CK(cudaMemcpy2DAsync(dst, pitch, src, pitch, width, r1, cudaMemcpyHostToDevice, ctx->copy));
+            for (int k = 1; k < parts; ++k)
+                if (height * (k + 1) / parts > height * k / parts)
+                    CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_join[k - 1], 0));
+            if (timed) prof_close(ctx, 1, ctx->copy, (double)(width * height));
+            ctx->st.h2d_bytes_t1_stream += (int64_t)(width * height);
+            goto t1_done;
+        }
+        {
         // rows [0, h_ce) by the copy engine, [h_ce, height) by the copy kernel
         const int h_ce = mode == TKV_T1_COPY_ENGINE ? height : mode == TKV_T1_SM_COPY ? 0 : height / 2;
-        const bool timed = prof_open(ctx, 1, ctx->copy);
         if (h_ce < height) {
             cudaStream_t ks = ctx->copy;
             if (h_ce > 0) {
@@ -335,7 +366,9 @@ tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
         if (h_ce > 0 && h_ce < height) CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_split, 0));
         if (timed) prof_close(ctx, 1, ctx->copy, (double)(width * height));
         ctx->st.h2d_bytes_t1_stream += (int64_t)(width * height);
+        }
     }
+t1_done:
     if (ctx->delta_max > 0) {
         tkv_status r = enqueue_delta(ctx, layer, layer + 1, ctx->copy);
         if (r != TKV_OK) return r;
@@ -373,7 +406,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     if (c.max_tokens < 1 || c.max_tokens > 65536) return TKV_EINVAL;
     if (c.prompt_len < 0 || c.num_sinks < 0 || c.recent_window < 0) return TKV_EINVAL;
     if (c.t0_capacity < 0 || c.t1_capacity < 0 || c.t2_capacity < 0) return TKV_EINVAL;
-    if (c.t1_transport < TKV_T1_COPY_ENGINE || c.t1_transport > TKV_T1_SPLIT) return TKV_EINVAL;
+    if (c.t1_transport < TKV_T1_COPY_ENGINE || c.t1_transport > TKV_T1_MULTI_CE) return TKV_EINVAL;
     const float r[4] = {c.ratio_t0, c.ratio_t1, c.ratio_t2, c.ratio_t3};
     int64_t ppm[4], sum = 0;
     for (int i = 0; i < 4; ++i) {
@@ -486,6 +519,10 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     E(cudaEventCreateWithFlags(&ctx->ev_retier, cudaEventDisableTiming));
     E(cudaEventCreateWithFlags(&ctx->ev_split, cudaEventDisableTiming));
     E(cudaStreamCreateWithFlags(&ctx->copy2, cudaStreamNonBlocking));
+    for (int i = 0; i < tkv_ctx::kCopyLanes - 1; ++i) {
+        E(cudaStreamCreateWithFlags(&ctx->copyx[i], cudaStreamNonBlocking));
+        E(cudaEventCreateWithFlags(&ctx->ev_join[i], cudaEventDisableTiming));
+    }
     if (!e) {
         (void)cudaGetLastError();
         return bail(TKV_ECUDA);
