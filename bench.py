@@ -269,6 +269,8 @@ def run_gpu(args, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ctx.profile_begin()
+    # marks the timed region for a profiler started with collection off (no-op otherwise)
+    torch.cuda.profiler.start()
     for i in range(args.steps):
         t += 1
         flush.fill_(i & 0xFF)
@@ -277,6 +279,7 @@ def run_gpu(args, rank, world):
         ev[i][1].record(stream)
     prof = ctx.profile_end()
     torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None

@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     uint32_t* rl_s = reinterpret_cast<uint32_t*>(smem + C::off_rl);
     int* n_s = reinterpret_cast<int*>(smem + C::off_n);
 
+    // the combine kernel may be scheduled once every CTA of this grid has started
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int IT = a.item_rows, IPG = a.items_per_group;
     const int total_items = a.B * a.Hkv * IPG;
@@ -95,18 +97,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     uint8_t* ring = smem + C::off_ring + (size_t)warp * C::sz_warp_ring;
     float* p_s = reinterpret_cast<float*>(smem + C::off_p) + (size_t)warp * kRows * 2 * GP;
 
-    // rows of every item of this CTA, and their retained-list slices
+    // Prologue in one round trip: the rows of every item, the retained-list slices
+    // (read up to the item size, clamped to the capacity; entries past the count
+    // are never used) and the first group's q.
     for (int item = it0 + tid; item < it1; item += NT) {
         const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
         n_s[item - it0] = max(0, min(IT, a.rl_count[b] - j0));
     }
-    __syncthreads();
     for (int item = it0; item < it1; ++item) {
         const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
-        const int n = n_s[item - it0];
+        const int cap = min(IT, a.Nmax - j0);
         const uint32_t* src = a.rl_loc + (size_t)b * a.Nmax + j0;
         uint32_t* dst = rl_s + (size_t)(item - it0) * IT;
-        for (int r = tid; r < n; r += NT) dst[r] = src[r];
+        for (int r = tid; r < cap; r += NT) dst[r] = src[r];
+    }
+    {
+        const int g = it0 / IPG, b = g / a.Hkv, kvh = g % a.Hkv;
+        for (int i = tid; i < G * D; i += NT)
+            q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kvh * G) * D + i]) * a.qscale;
     }
     __syncthreads();
     // tiles of this warp in an item: warp, warp + 4, ... below ceil(n / 32)
@@ -252,11 +260,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         const int j0 = (item % IPG) * IT;
         const int n = n_s[item - it0];
         if (g != cur_group) {
-            if (cur_group >= 0) flush_segment(cur_group);
-            else __syncthreads();
-            for (int i = tid; i < G * D; i += NT)
-                q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kvh * G) * D + i]) * a.qscale;
-            __syncthreads();
+            if (cur_group >= 0) {
+                flush_segment(cur_group);
+                for (int i = tid; i < G * D; i += NT)
+                    q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kvh * G) * D + i]) * a.qscale;
+                __syncthreads();
+            }
             reset_segment();
             cur_group = g;
         }
@@ -424,40 +433,64 @@ template <int G, int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
     constexpr int GP = C::GP, PS = C::PS;
-    extern __shared__ __align__(16) float fsm[];     // f[segment][8]
+    extern __shared__ __align__(16) float fsm[];     // m[seg][8], l[seg][8], then f[seg][8]
     __shared__ float Ms[8], Linv[8];
+    // launched as a programmatic dependent of the main kernel: wait for its results
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g = blockIdx.y, b = g / a.Hkv, kvh = g % a.Hkv;
     const int R = a.rl_count[b];
     const int IPG = a.items_per_group, ipc = a.items_per_cta;
     const int c_lo = (g * IPG) / ipc, c_hi = ((g + 1) * IPG - 1) / ipc;
     const int ns = c_hi - c_lo + 1;
-    auto rec = [&](int s) {
-        const int c = c_lo + s;
+    float* m_s = fsm;
+    float* l_s = fsm + ns * 8;
+    float* f_s = fsm + 2 * ns * 8;
+    auto rec = [&](int sg) {
+        const int c = c_lo + sg;
         const int seg = g - (c * ipc) / IPG;
         return a.part + ((size_t)c * a.part_segments + seg) * PS;
     };
+    // every segment's (m, l), gathered in parallel
+    for (int t = threadIdx.x; t < ns * 8; t += blockDim.x) {
+        const int sg = t >> 3, h = t & 7;
+        const float* r = rec(sg);
+        m_s[t] = h < G ? r[h] : -INFINITY;
+        l_s[t] = h < G ? r[8 + h] : 0.f;
+    }
+    __syncthreads();
     if (threadIdx.x < G) {
         const int h = threadIdx.x;
         float M = -INFINITY;
-        for (int s = 0; s < ns; ++s) M = fmaxf(M, rec(s)[h]);
+        for (int sg = 0; sg < ns; ++sg) M = fmaxf(M, m_s[sg * 8 + h]);
         float L = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const float ms = rec(s)[h];
+        for (int sg = 0; sg < ns; ++sg) {
+            const float ms = m_s[sg * 8 + h];
             const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-            fsm[s * 8 + h] = f;
-            L += f * rec(s)[8 + h];
+            f_s[sg * 8 + h] = f;
+            L += f * l_s[sg * 8 + h];
         }
         const float inv = 1.0f / L;
-        for (int s = 0; s < ns; ++s) fsm[s * 8 + h] *= inv;
+        for (int sg = 0; sg < ns; ++sg) f_s[sg * 8 + h] *= inv;
         Ms[h] = M;
         Linv[h] = inv;
     }
     __syncthreads();
-    if (blockIdx.x == 0) {
-        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    // out: the group's G * D elements are spread over its blocks; a thread issues the
+    // loads of up to 32 segments together, then sums in segment order
+    {
+        const int per = (G * D + gridDim.x - 1) / gridDim.x;
+        const int i0 = blockIdx.x * per, i1 = min(G * D, i0 + per);
+        for (int idx = i0 + threadIdx.x; idx < i1; idx += blockDim.x) {
             const int h = idx / D;
             float acc = 0.f;
-            for (int s = 0; s < ns; ++s) acc += rec(s)[16 + idx] * fsm[s * 8 + h];
+            for (int s0 = 0; s0 < ns; s0 += 32) {
+                float v[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] = (s0 + k < ns) ? rec(s0 + k)[16 + idx] : 0.f;
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (s0 + k < ns) acc += v[k] * f_s[(s0 + k) * 8 + h];
+            }
             a.out[((size_t)b * a.Hq + (size_t)kvh * G) * D + idx] = acc;
         }
     }
@@ -487,10 +520,18 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int rmax_blocks = (a.items_per_group * a.item_rows + kCombineRows - 1) / kCombineRows;
-    dim3 grid(rmax_blocks, a.B * a.Hkv);
     const int max_segs = (a.items_per_group + a.items_per_cta - 1) / a.items_per_cta + 1;
-    attn_combine_kernel<G, D><<<grid, 256, (size_t)max_segs * 8 * 4, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rmax_blocks, a.B * a.Hkv);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)max_segs * 3 * 8 * 4;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel<G, D>, a);
 }
 
 template <int G, int D>
