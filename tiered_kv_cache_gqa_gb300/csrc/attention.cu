@@ -43,7 +43,7 @@ namespace tkv {
 constexpr int kAttnWarps = 4;
 constexpr int kWarpStages = 2;
 constexpr int kMaxWindowRows = 4096;       // retained-list rows a CTA stages in shared memory
-constexpr int kCombineRows = 1024;         // rows per combine block
+constexpr int kCombineRows = 256;          // alpha rows per combine block (one per thread)
 
 template <int G, int D>
 struct AttnCfg {
@@ -111,11 +111,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         uint32_t* dst = rl_s + (size_t)(item - it0) * IT;
         for (int r = tid; r < cap; r += NT) dst[r] = src[r];
     }
-    {
-        const int g = it0 / IPG, b = g / a.Hkv, kvh = g % a.Hkv;
-        for (int i = tid; i < G * D; i += NT)
-            q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kvh * G) * D + i]) * a.qscale;
-    }
+    // q of group g, scaled, into shared memory: 8 elements per 16-byte load when q is aligned
+    auto load_q = [&](int g) {
+        const int b = g / a.Hkv, kvh = g % a.Hkv;
+        const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
+        if ((reinterpret_cast<uintptr_t>(qg) & 15u) == 0) {
+            for (int i = tid; i < G * D / 8; i += NT) {
+                const uint4 w = reinterpret_cast<const uint4*>(qg)[i];
+                const float2 f0 = bf16x2_to_float2(w.x), f1 = bf16x2_to_float2(w.y);
+                const float2 f2 = bf16x2_to_float2(w.z), f3 = bf16x2_to_float2(w.w);
+                float4* dst = reinterpret_cast<float4*>(q_s + 8 * i);
+                dst[0] = make_float4(f0.x * a.qscale, f0.y * a.qscale, f1.x * a.qscale, f1.y * a.qscale);
+                dst[1] = make_float4(f2.x * a.qscale, f2.y * a.qscale, f3.x * a.qscale, f3.y * a.qscale);
+            }
+        } else {
+            for (int i = tid; i < G * D; i += NT) q_s[i] = __bfloat162float(qg[i]) * a.qscale;
+        }
+    };
+    load_q(it0 / IPG);
     __syncthreads();
     // tiles of this warp in an item: warp, warp + 4, ... below ceil(n / 32)
     auto warp_tiles = [&](int n) {
@@ -262,8 +275,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         if (g != cur_group) {
             if (cur_group >= 0) {
                 flush_segment(cur_group);
-                for (int i = tid; i < G * D; i += NT)
-                    q_s[i] = __bfloat162float(a.q[((size_t)b * a.Hq + (size_t)kvh * G) * D + i]) * a.qscale;
+                load_q(g);
                 __syncthreads();
             }
             reset_segment();
@@ -428,17 +440,20 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
 
 // Merges a group's partials (one per CTA whose range touches the group, in CTA
 // order) into `out`, and writes the per-position sum over the group's query
-// heads of alpha = 2^(z - M) / L.
+// heads of alpha = 2^(z - M) / L.  Every load of the block is issued before the
+// first barrier (the segment statistics, the block's share of the partial
+// outputs, the logits of its rows), so the kernel costs about one memory round
+// trip after the main kernel ends.
 template <int G, int D>
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
     constexpr int GP = C::GP, PS = C::PS;
+    constexpr int kSegBatch = 32;                    // partial outputs loaded per thread at once
     extern __shared__ __align__(16) float fsm[];     // m[seg][8], l[seg][8], then f[seg][8]
     __shared__ float Ms[8], Linv[8];
     // launched as a programmatic dependent of the main kernel: wait for its results
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g = blockIdx.y, b = g / a.Hkv, kvh = g % a.Hkv;
-    const int R = a.rl_count[b];
     const int IPG = a.items_per_group, ipc = a.items_per_cta;
     const int c_lo = (g * IPG) / ipc, c_hi = ((g + 1) * IPG - 1) / ipc;
     const int ns = c_hi - c_lo + 1;
@@ -450,14 +465,34 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
         const int seg = g - (c * ipc) / IPG;
         return a.part + ((size_t)c * a.part_segments + seg) * PS;
     };
-    // every segment's (m, l), gathered in parallel
+    // (1) loads: segment statistics, this thread's first batch of partial outputs, its logits
     for (int t = threadIdx.x; t < ns * 8; t += blockDim.x) {
         const int sg = t >> 3, h = t & 7;
         const float* r = rec(sg);
         m_s[t] = h < G ? r[h] : -INFINITY;
         l_s[t] = h < G ? r[8 + h] : 0.f;
     }
+    const int per = (G * D + gridDim.x - 1) / gridDim.x;
+    const int i0 = blockIdx.x * per, i1 = min(G * D, i0 + per);
+    const int idx = i0 + threadIdx.x;                // blockDim.x >= per: one element per thread
+    const bool has_out = idx < i1;
+    float v[kSegBatch];
+#pragma unroll
+    for (int k = 0; k < kSegBatch; ++k) v[k] = (has_out && k < ns) ? rec(k)[16 + idx] : 0.f;
+    const int j = blockIdx.x * kCombineRows + threadIdx.x;
+    const bool has_row = j < a.Nmax;
+    float zz[GP];
+    if (has_row) {
+        const float* zg = a.zs + (((size_t)b * a.Hkv + kvh) * a.Nmax + j) * GP;
+#pragma unroll
+        for (int h = 0; h < GP; h += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(zg + h);
+            zz[h] = t.x; zz[h + 1] = t.y; zz[h + 2] = t.z; zz[h + 3] = t.w;
+        }
+    }
+    const int R = a.rl_count[b];
     __syncthreads();
+    // (2) the group's M and L per head, and every segment's factor 2^(m - M) / L
     if (threadIdx.x < G) {
         const int h = threadIdx.x;
         float M = -INFINITY;
@@ -475,39 +510,28 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
         Linv[h] = inv;
     }
     __syncthreads();
-    // out: the group's G * D elements are spread over its blocks; a thread issues the
-    // loads of up to 32 segments together, then sums in segment order
-    {
-        const int per = (G * D + gridDim.x - 1) / gridDim.x;
-        const int i0 = blockIdx.x * per, i1 = min(G * D, i0 + per);
-        for (int idx = i0 + threadIdx.x; idx < i1; idx += blockDim.x) {
-            const int h = idx / D;
-            float acc = 0.f;
-            for (int s0 = 0; s0 < ns; s0 += 32) {
-                float v[32];
+    // (3) out, summed in segment order; groups with more than kSegBatch segments load the rest now
+    if (has_out) {
+        const int h = idx / D;
+        float acc = 0.f;
 #pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = (s0 + k < ns) ? rec(s0 + k)[16 + idx] : 0.f;
+        for (int k = 0; k < kSegBatch; ++k)
+            if (k < ns) acc += v[k] * f_s[k * 8 + h];
+        for (int s0 = kSegBatch; s0 < ns; s0 += kSegBatch) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (s0 + k < ns) acc += v[k] * f_s[(s0 + k) * 8 + h];
-            }
-            a.out[((size_t)b * a.Hq + (size_t)kvh * G) * D + idx] = acc;
+            for (int k = 0; k < kSegBatch; ++k) v[k] = (s0 + k < ns) ? rec(s0 + k)[16 + idx] : 0.f;
+#pragma unroll
+            for (int k = 0; k < kSegBatch; ++k)
+                if (s0 + k < ns) acc += v[k] * f_s[(s0 + k) * 8 + h];
         }
+        a.out[((size_t)b * a.Hq + (size_t)kvh * G) * D + idx] = acc;
     }
-    const float* zg = a.zs + ((size_t)b * a.Hkv + kvh) * a.Nmax * GP;
-    float* gdst = a.g + (((size_t)a.layer * a.B + b) * a.Hkv + kvh) * a.Nmax;
-    const int j_end = min(R, (int)(blockIdx.x + 1) * kCombineRows);
-    for (int j = blockIdx.x * kCombineRows + threadIdx.x; j < j_end; j += blockDim.x) {
-        float zz[GP];
-#pragma unroll
-        for (int h = 0; h < GP; h += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(zg + (size_t)j * GP + h);
-            zz[h] = t.x; zz[h + 1] = t.y; zz[h + 2] = t.z; zz[h + 3] = t.w;
-        }
+    // (4) alpha sums of this block's rows
+    if (has_row && j < R) {
         float acc = 0.f;
 #pragma unroll
         for (int h = 0; h < G; ++h) acc += exp2f(zz[h] - Ms[h]) * Linv[h];
-        gdst[j] = acc;
+        a.g[(((size_t)a.layer * a.B + b) * a.Hkv + kvh) * a.Nmax + j] = acc;
     }
 }
 
@@ -519,12 +543,19 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
     attn_kernel<G, D><<<a.grid, kAttnWarps * 32, smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int rmax_blocks = (a.items_per_group * a.item_rows + kCombineRows - 1) / kCombineRows;
+    // one alpha row per thread; enough blocks that every block holds at most 256 out elements
+    const int rows = a.items_per_group * a.item_rows;
+    const int blocks = std::max((rows + kCombineRows - 1) / kCombineRows, (G * D + kCombineRows - 1) / kCombineRows);
     const int max_segs = (a.items_per_group + a.items_per_cta - 1) / a.items_per_cta + 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rmax_blocks, a.B * a.Hkv);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.gridDim = dim3(blocks, a.B * a.Hkv);
+    cfg.blockDim = dim3(kCombineRows, 1, 1);
     cfg.dynamicSmemBytes = (size_t)max_segs * 3 * 8 * 4;
+    if (cfg.dynamicSmemBytes > 48 * 1024) {
+        e = cudaFuncSetAttribute(attn_combine_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
