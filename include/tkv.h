@@ -136,12 +136,16 @@ void tkv_destroy(tkv_ctx* ctx);
 /* Appends n_tokens new positions for one layer ("Four-tier classification":
  * new tokens fall in the recent window, so they enter T0).
  * k, v: device bf16 [B][n_tokens][Hkv][d].
+ * k and v must be 16-byte aligned.
  * Protocol: a group of n tokens opens with layer 0 and every layer is
  * appended in order 0..L-1.  With n_tokens == 1 the group is a decode step:
  * tkv_decode_step(layer) follows tkv_append(layer), and the step closes after
- * tkv_decode_step(L-1).  With n_tokens > 1 (prefill) the positions are
- * committed when layer L-1 is appended; pre-filled positions start with
- * s = 0 and are not scored.
+ * tkv_decode_step(L-1).  A decode token's rows are written into T0 by the
+ * attention kernel of that tkv_decode_step (no launch of their own), so k and v
+ * must stay valid and unchanged until that call's work has run on the compute
+ * stream.  With n_tokens > 1 (prefill) the rows are copied on the compute
+ * stream at once and the positions are committed when layer L-1 is appended;
+ * pre-filled positions start with s = 0 and are not scored.
  * Errors: TKV_EINVAL (layer out of order, NULL pointers, n_tokens < 1),
  * TKV_ECAPACITY (max_tokens or T0 capacity would be exceeded; nothing changes). */
 tkv_status tkv_append(tkv_ctx* ctx, int32_t layer, const void* k, const void* v,

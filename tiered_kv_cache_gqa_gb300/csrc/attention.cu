@@ -130,6 +130,27 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     };
     load_q(it0 / IPG);
     __syncthreads();
+    // The decode token of each group is its last retained row (T0).  The CTA whose
+    // items hold it writes its K and V into the T0 slot before any row is streamed.
+    if (a.new_k != nullptr) {
+        for (int item = it0; item < it1; ++item) {
+            const int g = item / IPG, b = g / a.Hkv, kvh = g % a.Hkv, j0 = (item % IPG) * IT;
+            const int jl = a.rl_count[b] - 1 - j0;
+            if (jl < 0 || jl >= IT) continue;
+            const int slot = loc_slot(rl_s[(size_t)(item - it0) * IT + jl]);
+            constexpr int CH = D / 8;                  // 16-byte chunks per row
+            if (tid < 2 * CH) {
+                const int kv = tid / CH, c = tid % CH;
+                const __nv_bfloat16* src = (kv ? a.new_v : a.new_k) + ((size_t)b * a.Hkv + kvh) * D;
+                const uint4 w = reinterpret_cast<const uint4*>(src)[c];
+                // the T0 pool is read-only to the kernel except for this row
+                __nv_bfloat16* dst = const_cast<__nv_bfloat16*>(a.k0v0) +
+                                     row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S0) * D;
+                reinterpret_cast<uint4*>(dst)[c] = w;
+            }
+        }
+        __syncthreads();   // the stores above are visible to the copies this CTA issues next
+    }
     // tiles of this warp in an item: warp, warp + 4, ... below ceil(n / 32)
     auto warp_tiles = [&](int n) {
         const int nt = (n + kRows - 1) / kRows;
@@ -677,13 +698,32 @@ size_t attention_zs_floats(int G, int B, int Hkv, int Nmax) {
 __global__ void fold_kernel(const float* __restrict__ g, const int32_t* __restrict__ rl_pos,
                             const int32_t* __restrict__ rl_count, float* __restrict__ s, int L,
                             int B, int Hkv, int Nmax, float inv_lh) {
+    constexpr int kBatch = 16;   // loads in flight per thread
     const int b = blockIdx.y;
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= rl_count[b]) return;
-    float acc = 0.f;
-    for (int l = 0; l < L; ++l)
-        for (int h = 0; h < Hkv; ++h) acc += g[(((size_t)l * B + b) * Hkv + h) * Nmax + j];
     const int pos = rl_pos[(size_t)b * Nmax + j];
+    // terms in (layer, head) order; (l, h) of term k0 + k follow by carries, no division
+    const int n = L * Hkv;
+    float acc = 0.f;
+    int l0 = 0, h0 = 0;
+    for (int k0 = 0; k0 < n; k0 += kBatch) {
+        float v[kBatch];
+        int l = l0, h = h0;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            v[k] = (k0 + k < n) ? g[(((size_t)l * B + b) * Hkv + h) * Nmax + j] : 0.f;
+            if (++h == Hkv) {
+                h = 0;
+                ++l;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+            if (k0 + k < n) acc += v[k];
+        l0 = l;
+        h0 = h;
+    }
     s[(size_t)b * Nmax + pos] += acc * inv_lh;
 }
 

@@ -68,6 +68,8 @@ struct tkv_ctx {
     // protocol state
     int open_n = 0, appended = 0, decoded = 0;
     std::vector<char> prefetched;
+    // decode-token rows appended but not yet written (the layer's attention kernel writes them)
+    std::vector<const void*> pend_k, pend_v;
     int delta_max = 0;                 // pending delta moves (max over sequences), 0 = none
 
     int resident = 1;                  // attention CTAs resident on the device at once
@@ -545,6 +547,8 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     for (int t = 0; t < 4; ++t) ctx->count[t].assign(B, 0);
     ctx->R.assign(B, 0);
     ctx->prefetched.assign(L, 0);
+    ctx->pend_k.assign(L, nullptr);
+    ctx->pend_v.assign(L, nullptr);
     *out = ctx;
     return TKV_OK;
 }
@@ -582,9 +586,15 @@ tkv_status tkv_append(tkv_ctx* ctx, int32_t layer, const void* k, const void* v,
     } else {
         if (n_tokens != ctx->open_n || layer != ctx->appended) return TKV_EINVAL;
     }
-    CK(launch_append_rows((const __nv_bfloat16*)k, (const __nv_bfloat16*)v, ctx->k0v0, ctx->slot, layer,
-                          B, ctx->Hkv, ctx->d, ctx->Nmax, ctx->S0, ctx->N, n_tokens, ctx->compute));
-    ctx->launches++;
+    if (n_tokens == 1) {
+        // written by this layer's attention kernel
+        ctx->pend_k[layer] = k;
+        ctx->pend_v[layer] = v;
+    } else {
+        CK(launch_append_rows((const __nv_bfloat16*)k, (const __nv_bfloat16*)v, ctx->k0v0, ctx->slot, layer,
+                              B, ctx->Hkv, ctx->d, ctx->Nmax, ctx->S0, ctx->N, n_tokens, ctx->compute));
+        ctx->launches++;
+    }
     ctx->appended++;
     if (ctx->open_n > 1 && ctx->appended == ctx->L) {
         ctx->N += ctx->open_n;
@@ -624,6 +634,9 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
     a.k0v0 = ctx->k0v0;
     a.stage = ctx->stage + (size_t)slotr * 2 * ctx->B * ctx->Hkv * ctx->S1 * ctx->d;
     a.t2 = ctx->t2;
+    a.new_k = (const __nv_bfloat16*)ctx->pend_k[layer];
+    a.new_v = (const __nv_bfloat16*)ctx->pend_v[layer];
+    ctx->pend_k[layer] = ctx->pend_v[layer] = nullptr;
     a.rl_loc = ctx->rl_loc;
     a.rl_count = ctx->rl_count;
     a.g = ctx->g;

@@ -157,6 +157,8 @@ struct AttnArgs {
     const __nv_bfloat16* k0v0;   // T0 pool (all layers)
     const __nv_bfloat16* stage;  // staging ring slot for this layer: [2][B][Hkv][S1][d]
     const uint8_t* t2;           // T2 pool (all layers)
+    const __nv_bfloat16* new_k;  // [B][Hkv][d] this layer's decode-token K, written to its T0 slot
+    const __nv_bfloat16* new_v;  //   by the CTA that owns the row (null: nothing to write)
     const uint32_t* rl_loc;      // [B][Nmax]
     const int32_t* rl_count;     // [B]
     float* g;                    // [L][B][Hkv][Nmax]  per-position alpha sums (written by the combine)
