@@ -257,10 +257,10 @@ tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t
  *   s:   device fp32 [B][R], read and updated in place: s += the step's mean
  *        over layers and query heads of the attention weights
  *   stream: cudaStream_t to enqueue on (NULL = the legacy default stream)
- * Scratch lives in fixed file-scope device arrays (about 22 MiB), held by
- * every GPU that loads the library until exit: L*B*Hkv*R <= 1,048,576,
- * B*Hkv*R <= 131,072, B*R <= 131,072, B <= 256; larger sizes return
- * TKV_ECAPACITY before anything is enqueued.
+ * Scratch lives in fixed file-scope device arrays (about 34 MiB), held by
+ * every GPU that loads the library until exit: B*Hkv*R <= 131,072,
+ * B*R <= 131,072, B <= 256; larger sizes return TKV_ECAPACITY before anything
+ * is enqueued.
  * It calls no cudaMalloc, cudaFree or other allocating routine.  The first
  * call on a device (with that device current) resolves the scratch addresses
  * and should come before any stream capture.  All calls share the scratch and

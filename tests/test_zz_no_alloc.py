@@ -58,8 +58,8 @@ def test_noalloc_matches_context_path_on_two_calls():
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     q = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(1, device="cuda")
-    # 64 layers * 8 sequences * 8 KV heads * 1024 positions > 2,097,152 attention-weight sums
-    rc = tkv.tkv_decode_dense_noalloc(q, q, out, out, 64, 8, 64, 8, 128, 1024)
+    # 16 sequences * 16 KV heads * 1024 positions > 131,072 retained (sequence, KV head, row) triples
+    rc = tkv.tkv_decode_dense_noalloc(q, q, out, out, 1, 16, 128, 16, 128, 1024)
     assert rc == tkv.TKV_ECAPACITY
     rc = tkv.tkv_decode_dense_noalloc(q, q, out, out, 1, 1, 64, 8, 96, 16)
     assert rc == tkv.TKV_EINVAL

@@ -61,7 +61,7 @@ struct AttnCfg {
     static constexpr size_t off_p = off_q + (size_t)G * D * 4;
     static constexpr size_t off_comb = off_p + (size_t)kAttnWarps * kRows * 2 * GP * 4;   // p as (p, p) pairs
     static constexpr size_t off_n = off_comb + (size_t)kAttnWarps * PS * 4;   // rows of each item
-    static constexpr size_t off_rl = off_n + (size_t)(kMaxWindowRows / 128) * 4;
+    static constexpr size_t off_rl = off_n + (size_t)(kMaxWindowRows / 128) * 2 * 4;   // + decode-token flags
 
     static size_t smem(int rl_rows) { return off_rl + (size_t)rl_rows * 4; }
 };
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     float* comb = reinterpret_cast<float*>(smem + C::off_comb);
     uint32_t* rl_s = reinterpret_cast<uint32_t*>(smem + C::off_rl);
     int* n_s = reinterpret_cast<int*>(smem + C::off_n);
+    int* own_s = n_s + kMaxWindowRows / 128;
 
     // the combine kernel may be scheduled once every CTA of this grid has started
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -102,7 +103,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     // are never used) and the first group's q.
     for (int item = it0 + tid; item < it1; item += NT) {
         const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
-        n_s[item - it0] = max(0, min(IT, a.rl_count[b] - j0));
+        const int R = a.rl_count[b];
+        n_s[item - it0] = max(0, min(IT, R - j0));
+        // the group's decode token (its last retained row) falls in this item
+        own_s[item - it0] = (a.new_k != nullptr && R - 1 >= j0 && R - 1 < j0 + IT) ? 1 : 0;
     }
     for (int item = it0; item < it1; ++item) {
         const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
@@ -130,31 +134,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     };
     load_q(it0 / IPG);
     __syncthreads();
-    // The decode token of each group is its last retained row (T0).  The CTA whose
-    // items hold it writes its K and V into the T0 slot before any row is streamed.
-    if (a.new_k != nullptr) {
-        for (int item = it0; item < it1; ++item) {
-            const int g = item / IPG, b = g / a.Hkv, kvh = g % a.Hkv, j0 = (item % IPG) * IT;
-            const int jl = a.rl_count[b] - 1 - j0;
-            if (jl < 0 || jl >= IT) continue;
-            const int slot = loc_slot(rl_s[(size_t)(item - it0) * IT + jl]);
-            constexpr int CH = D / 8;                  // 16-byte chunks per row
-            if (tid < 2 * CH) {
-                const int kv = tid / CH, c = tid % CH;
-                const __nv_bfloat16* src = (kv ? a.new_v : a.new_k) + ((size_t)b * a.Hkv + kvh) * D;
-                const uint4 w = reinterpret_cast<const uint4*>(src)[c];
-                // the T0 pool is read-only to the kernel except for this row
-                __nv_bfloat16* dst = const_cast<__nv_bfloat16*>(a.k0v0) +
-                                     row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S0) * D;
-                reinterpret_cast<uint4*>(dst)[c] = w;
-            }
-        }
-        __syncthreads();   // the stores above are visible to the copies this CTA issues next
-    }
     // tiles of this warp in an item: warp, warp + 4, ... below ceil(n / 32)
     auto warp_tiles = [&](int n) {
         const int nt = (n + kRows - 1) / kRows;
         return warp < nt ? (nt - warp + kAttnWarps - 1) / kAttnWarps : 0;
+    };
+
+    // row (within tile `tile` of item) of the group's decode token, or -1
+    auto new_row_in = [&](int item, int tile) {
+        const int n = n_s[item - it0];
+        const int r = n - 1 - tile * kRows;
+        return (own_s[item - it0] && r >= 0 && r < kRows) ? r : -1;
     };
 
     // ------------------------------------------------------------ issue side
@@ -199,6 +189,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                     row_v = a.t2 + row_index(a.layer, 1, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
                     row_bytes = D + 16;
                     fp8 = true;
+                }
+                if (lane == new_row_in(item, tile)) {
+                    // not in its T0 slot yet: stream it from the caller's rows
+                    src = reinterpret_cast<const uint8_t*>(a.new_k + ((size_t)b * a.Hkv + kvh) * D);
+                    row_v = reinterpret_cast<const uint8_t*>(a.new_v + ((size_t)b * a.Hkv + kvh) * D);
                 }
             }
             fp8_mask_issue = __ballot_sync(0xffffffffu, fp8);
@@ -315,6 +310,18 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
             const uint32_t tmask = fp8_mask_issue;
             cp_async_wait_prev();
             __syncwarp();
+            // the decode token's rows go from the ring into their T0 slot (K now, V below)
+            const int newr = new_row_in(item, tile);
+            auto store_new_row = [&](int kv) {
+                if (lane < 2 * D / 16) {
+                    const int slot = loc_slot(rl_s[(size_t)(item - it0) * IT + tile * kRows + newr]);
+                    const uint8_t* srow = ring + (size_t)(consumed % kWarpStages) * C::sz_stage + (size_t)newr * ROWB;
+                    uint8_t* drow = reinterpret_cast<uint8_t*>(const_cast<__nv_bfloat16*>(a.k0v0)) +
+                                    row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S0) * (2 * D);
+                    reinterpret_cast<uint4*>(drow)[lane] = reinterpret_cast<const uint4*>(srow)[lane];
+                }
+            };
+            if (newr >= 0) store_new_row(0);
             float z[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) z[h] = -INFINITY;
@@ -405,6 +412,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
             cp_async_commit();
             cp_async_wait_prev();
             __syncwarp();
+            if (newr >= 0) store_new_row(1);
             {
                 const int nrows = min(kRows, n - tile * kRows);
                 const uint8_t* stage = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
@@ -512,6 +520,9 @@ __global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) 
         }
     }
     const int R = a.rl_count[b];
+    // running sum over layers of this row's alpha (layer 0 starts it)
+    float* gj = a.g + ((size_t)b * a.Hkv + kvh) * a.Nmax + j;
+    const float g_prev = (has_row && a.layer > 0) ? *gj : 0.f;
     __syncthreads();
     // (2) the group's M and L per head, and every segment's factor 2^(m - M) / L
     if (threadIdx.x < G) {
@@ -552,7 +563,7 @@ __global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) 
         float acc = 0.f;
 #pragma unroll
         for (int h = 0; h < G; ++h) acc += exp2f(zz[h] - Ms[h]) * Linv[h];
-        a.g[(((size_t)a.layer * a.B + b) * a.Hkv + kvh) * a.Nmax + j] = acc;
+        *gj = g_prev + acc;
     }
 }
 
@@ -694,44 +705,25 @@ size_t attention_zs_floats(int G, int B, int Hkv, int Nmax) {
 }
 
 // ---------------------------------------------------------------- score fold
-// s[b][pos(j)] += (sum_l sum_kvh g[l][b][kvh][j]) / (L * Hq), fixed order.
+// s[b][pos(j)] += (sum_kvh g[b][kvh][j]) / (L * Hq), g holding each (KV head,
+// row)'s sum over layers and that head's query heads of alpha; fixed order.
 __global__ void fold_kernel(const float* __restrict__ g, const int32_t* __restrict__ rl_pos,
-                            const int32_t* __restrict__ rl_count, float* __restrict__ s, int L,
-                            int B, int Hkv, int Nmax, float inv_lh) {
-    constexpr int kBatch = 16;   // loads in flight per thread
+                            const int32_t* __restrict__ rl_count, float* __restrict__ s, int Hkv,
+                            int Nmax, float inv_lh) {
     const int b = blockIdx.y;
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= rl_count[b]) return;
     const int pos = rl_pos[(size_t)b * Nmax + j];
-    // terms in (layer, head) order; (l, h) of term k0 + k follow by carries, no division
-    const int n = L * Hkv;
     float acc = 0.f;
-    int l0 = 0, h0 = 0;
-    for (int k0 = 0; k0 < n; k0 += kBatch) {
-        float v[kBatch];
-        int l = l0, h = h0;
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            v[k] = (k0 + k < n) ? g[(((size_t)l * B + b) * Hkv + h) * Nmax + j] : 0.f;
-            if (++h == Hkv) {
-                h = 0;
-                ++l;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k)
-            if (k0 + k < n) acc += v[k];
-        l0 = l;
-        h0 = h;
-    }
+    for (int h = 0; h < Hkv; ++h) acc += g[((size_t)b * Hkv + h) * Nmax + j];
     s[(size_t)b * Nmax + pos] += acc * inv_lh;
 }
 
 cudaError_t launch_fold(const float* g, const int32_t* rl_pos, const int32_t* rl_count, float* s,
-                        int L, int B, int Hkv, int Nmax, int rmax, float inv_lh, cudaStream_t st) {
+                        int B, int Hkv, int Nmax, int rmax, float inv_lh, cudaStream_t st) {
     if (rmax <= 0) return cudaSuccess;
     dim3 grid((rmax + 255) / 256, B);
-    fold_kernel<<<grid, 256, 0, st>>>(g, rl_pos, rl_count, s, L, B, Hkv, Nmax, inv_lh);
+    fold_kernel<<<grid, 256, 0, st>>>(g, rl_pos, rl_count, s, Hkv, Nmax, inv_lh);
     return cudaGetLastError();
 }
 

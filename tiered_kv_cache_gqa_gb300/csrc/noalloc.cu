@@ -26,8 +26,8 @@ using namespace tkv;
 
 namespace {
 
-constexpr size_t kMaxAlphaFloats = size_t(1) << 20;   // L*B*Hkv*R  <= 1,048,576  (4 MiB)
 constexpr size_t kMaxGroupRows = size_t(1) << 17;     // B*Hkv*R    <= 131,072
+constexpr size_t kMaxAlphaFloats = kMaxGroupRows;     // per-row alpha sums over layers (0.5 MiB)
 constexpr size_t kMaxTable = size_t(1) << 17;         // B*R        <= 131,072    (0.5 MiB)
 constexpr int kMaxBatch = 256;
 constexpr size_t kMaxZsFloats = kMaxGroupRows * 8;    // logits, 8 per row      (4 MiB)
@@ -96,8 +96,7 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
     if (L < 1 || B < 1 || Hkv < 1 || Hq < 1 || R < 1 || Hq % Hkv || Hq / Hkv > 8 || (d != 64 && d != 128))
         return TKV_EINVAL;
     // size limits of the fixed scratch
-    if (B > kMaxBatch || (size_t)B * R > kMaxTable || (size_t)B * Hkv * R > kMaxGroupRows ||
-        (size_t)L * B * Hkv * R > kMaxAlphaFloats)
+    if (B > kMaxBatch || (size_t)B * R > kMaxTable || (size_t)B * Hkv * R > kMaxGroupRows)
         return TKV_ECAPACITY;
 
     int dev = 0;
@@ -153,7 +152,7 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
         }
     }
     const float inv = (float)(1.0 / ((double)L * (double)Hq));
-    if (launch_fold(sc->alpha, (const int32_t*)sc->index, sc->count, s, L, B, Hkv, R, R, inv, st) !=
+    if (launch_fold(sc->alpha, (const int32_t*)sc->index, sc->count, s, B, Hkv, R, R, inv, st) !=
         cudaSuccess) {
         (void)cudaGetLastError();
         return TKV_ECUDA;

@@ -472,7 +472,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     A(dalloc(ctx, &ctx->rl_loc, B * Nmax));
     A(dalloc(ctx, &ctx->rl_pos, B * Nmax));
     A(dalloc(ctx, &ctx->rl_count, B));
-    A(dalloc(ctx, &ctx->g, L * B * Hkv * Nmax));
+    A(dalloc(ctx, &ctx->g, B * Hkv * Nmax));
     A(dalloc(ctx, &ctx->zs, attention_zs_floats(G, (int)B, (int)Hkv, (int)Nmax)));
     A(dalloc(ctx, &ctx->t0_free, B * S0));
     A(dalloc(ctx, &ctx->t0_top, B));
@@ -666,7 +666,7 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
     ctx->decoded++;
     if (ctx->decoded == ctx->L) {
         const float inv = (float)(1.0 / ((double)ctx->L * (double)ctx->Hq));
-        CK(launch_fold(ctx->g, ctx->rl_pos, ctx->rl_count, ctx->s, ctx->L, ctx->B, ctx->Hkv, ctx->Nmax, rmax,
+        CK(launch_fold(ctx->g, ctx->rl_pos, ctx->rl_count, ctx->s, ctx->B, ctx->Hkv, ctx->Nmax, rmax,
                        inv, ctx->compute));
         ctx->launches++;
         ctx->N += 1;

@@ -161,7 +161,7 @@ struct AttnArgs {
     const __nv_bfloat16* new_v;  //   by the CTA that owns the row (null: nothing to write)
     const uint32_t* rl_loc;      // [B][Nmax]
     const int32_t* rl_count;     // [B]
-    float* g;                    // [L][B][Hkv][Nmax]  per-position alpha sums (written by the combine)
+    float* g;                    // [B][Hkv][Nmax] per-position alpha sums, running over the step's layers
     float* part;                 // [grid][part_segments][16 + G*d] softmax partials per (CTA, group) (scratch)
     float* zs;                   // [B][Hkv][Nmax][GP] logits, log2-scaled (scratch)
     int32_t* err;                // status word (unused by kernels without device waits)
@@ -192,7 +192,7 @@ int attention_resident_ctas(int G, int d, size_t smem);                  // CTAs
 cudaError_t attention_ensure_smem(int G, int d, size_t smem);   // raises the cap, never lowers it
 
 cudaError_t launch_fold(const float* g, const int32_t* rl_pos, const int32_t* rl_count, float* s,
-                        int L, int B, int Hkv, int Nmax, int rmax, float inv_lh, cudaStream_t st);
+                        int B, int Hkv, int Nmax, int rmax, float inv_lh, cudaStream_t st);
 
 cudaError_t launch_open(int32_t* t0_free, int32_t* t0_top, uint8_t* tier, int32_t* slot, float* s,
                         uint32_t* rl_loc, int32_t* rl_pos, int32_t* rl_count, int B, int Nmax,
