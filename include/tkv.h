@@ -273,6 +273,27 @@ tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, float* out, f
                                     int32_t num_kv_heads, int32_t head_dim, int32_t num_positions,
                                     void* stream);
 
+/* CUDA-graph decode steps.  The pages have no counterpart: this is how a
+ * serving loop takes the host-side cost of the per-layer calls (and the gaps
+ * between launches) off a decode step.
+ * tkv_capture_begin: between decode steps, with no delta prefetch pending
+ * (i.e. not on the first step after a re-tier), profiling off and the T1
+ * transport TKV_T1_COPY_ENGINE or TKV_T1_SM_COPY.  The caller then makes one
+ * decode step's calls (tkv_append / tkv_prefetch / tkv_decode_step for every
+ * layer) as usual: they are recorded into a graph, on an internal stream, and
+ * nothing runs.  tkv_capture_end instantiates the graph, puts the context back
+ * to its state before the step and sets *steps_valid to the number of
+ * replays the graph stays valid for (the launch geometry covers the retained
+ * counts; capacity).  tkv_replay launches the graph on the compute stream: one
+ * decode step, with the pointers given at capture (the caller refills those
+ * buffers before each replay).  Any re-tier, tkv_set_tiers or prefill append
+ * discards the graph.
+ * Errors: TKV_EINVAL (call order, conditions above, no valid graph, the
+ * captured calls were not exactly one decode step), TKV_ECUDA. */
+tkv_status tkv_capture_begin(tkv_ctx* ctx);
+tkv_status tkv_capture_end(tkv_ctx* ctx, int32_t* steps_valid);
+tkv_status tkv_replay(tkv_ctx* ctx);
+
 /* Waits for all enqueued work and reports any device-side status word. */
 tkv_status tkv_sync(tkv_ctx* ctx);
 

@@ -25,7 +25,8 @@ TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY, TKV_T1_SPLIT, TKV_T1_MULTI_CE = range(4)
 EXPORTS = ("tkv_create", "tkv_destroy", "tkv_append", "tkv_prefetch", "tkv_decode_step",
            "tkv_retier", "tkv_get_scores", "tkv_set_scores", "tkv_get_tiers", "tkv_set_tiers",
            "tkv_get_row", "tkv_profile_begin", "tkv_profile_end", "tkv_sync", "tkv_get_stats",
-           "tkv_status_string", "tkv_decode_dense_noalloc")
+           "tkv_status_string", "tkv_decode_dense_noalloc", "tkv_capture_begin", "tkv_capture_end",
+           "tkv_replay")
 
 
 class TkvUnavailable(RuntimeError):
@@ -111,6 +112,9 @@ def load():
     lib.tkv_profile_end.argtypes = [vp, ctypes.POINTER(ProfEntry), ctypes.POINTER(ProfEntry),
                                     ctypes.POINTER(ProfEntry)]
     lib.tkv_decode_dense_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.tkv_capture_begin.argtypes = [vp]
+    lib.tkv_capture_end.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.tkv_replay.argtypes = [vp]
     lib.tkv_sync.argtypes = [vp]
     lib.tkv_get_stats.argtypes = [vp, ctypes.POINTER(Stats)]
     lib.tkv_status_string.argtypes = [st]
@@ -163,6 +167,21 @@ def tkv_decode_step(ctx, layer, q, out):
 
 def tkv_retier(ctx):
     return load().tkv_retier(ctx)
+
+
+def tkv_capture_begin(ctx):
+    return load().tkv_capture_begin(ctx)
+
+
+def tkv_capture_end(ctx):
+    """Returns (status, replays the captured step stays valid for)."""
+    n = ctypes.c_int32(0)
+    rc = load().tkv_capture_end(ctx, ctypes.byref(n))
+    return rc, int(n.value)
+
+
+def tkv_replay(ctx):
+    return load().tkv_replay(ctx)
 
 
 def tkv_get_scores(ctx, dst: np.ndarray):
@@ -292,6 +311,18 @@ class TieredKV:
 
     def retier(self):
         _check(tkv_retier(self.ctx), "tkv_retier")
+
+    def capture_begin(self):
+        _check(tkv_capture_begin(self.ctx), "tkv_capture_begin")
+
+    def capture_end(self):
+        """Ends a capture; returns how many replays the captured step stays valid for."""
+        rc, n = tkv_capture_end(self.ctx)
+        _check(rc, "tkv_capture_end")
+        return n
+
+    def replay(self):
+        _check(tkv_replay(self.ctx), "tkv_replay")
 
     def sync(self):
         _check(tkv_sync(self.ctx), "tkv_sync")

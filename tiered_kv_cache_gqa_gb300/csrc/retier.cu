@@ -441,38 +441,59 @@ cudaError_t launch_t1_copy(const void* src, void* dst, size_t pitch16, size_t wi
 // ------------------------------------------------------------ open / append
 // Opens n new positions [N, N+n) of every sequence in T0: pops T0 slots from
 // the free stack, resets s, appends to the retained list.
-__global__ void open_kernel(const int32_t* __restrict__ t0_free, const int32_t* __restrict__ t0_top,
-                            uint8_t* tier, int32_t* slot, float* s, uint32_t* rl_loc, int32_t* rl_pos,
-                            const int32_t* __restrict__ rl_count, int Nmax, int S0, int N, int n) {
+// Opens n new positions of every sequence: T0 slots from the free stack, tier
+// 0, s = 0, appended to the retained list.  The position counter lives on the
+// device (pos_n[b], equal for every b), so a captured decode step replays with
+// the right positions.  With n <= blockDim.x one block per sequence also
+// commits (pops the slots, grows the retained count, advances pos_n);
+// otherwise open_commit_kernel does, after every block has read the counters.
+__global__ void open_kernel(const int32_t* __restrict__ t0_free, int32_t* t0_top, uint8_t* tier, int32_t* slot,
+                            float* s, uint32_t* rl_loc, int32_t* rl_pos, int32_t* rl_count, int32_t* pos_n,
+                            int Nmax, int S0, int n, int commit) {
     const int b = blockIdx.y;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const int top = t0_top[b];
-    const int sl = t0_free[(size_t)b * S0 + top - 1 - i];
-    const size_t p = (size_t)b * Nmax + N + i;
-    tier[p] = 0;
-    slot[p] = sl;
-    s[p] = 0.f;
-    const size_t j = (size_t)b * Nmax + rl_count[b] + i;
-    rl_loc[j] = make_loc(0, sl);
-    rl_pos[j] = N + i;
+    const int top = t0_top[b], cnt = rl_count[b], N = pos_n[b];
+    if (i < n) {
+        const int sl = t0_free[(size_t)b * S0 + top - 1 - i];
+        const size_t p = (size_t)b * Nmax + N + i;
+        tier[p] = 0;
+        slot[p] = sl;
+        s[p] = 0.f;
+        const size_t j = (size_t)b * Nmax + cnt + i;
+        rl_loc[j] = make_loc(0, sl);
+        rl_pos[j] = N + i;
+    }
+    if (commit) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            t0_top[b] = top - n;
+            rl_count[b] = cnt + n;
+            pos_n[b] = N + n;
+        }
+    }
 }
 
-__global__ void open_commit_kernel(int32_t* t0_top, int32_t* rl_count, int B, int n) {
+__global__ void open_commit_kernel(int32_t* t0_top, int32_t* rl_count, int32_t* pos_n, int B, int n) {
     const int b = threadIdx.x;
     if (b < B) {
         t0_top[b] -= n;
         rl_count[b] += n;
+        pos_n[b] += n;
     }
 }
 
 cudaError_t launch_open(int32_t* t0_free, int32_t* t0_top, uint8_t* tier, int32_t* slot, float* s,
-                        uint32_t* rl_loc, int32_t* rl_pos, int32_t* rl_count, int B, int Nmax,
-                        int S0, int N, int n, cudaStream_t st) {
+                        uint32_t* rl_loc, int32_t* rl_pos, int32_t* rl_count, int32_t* pos_n, int B, int Nmax,
+                        int S0, int n, cudaStream_t st, int* launches) {
     dim3 grid((n + 255) / 256, B);
-    open_kernel<<<grid, 256, 0, st>>>(t0_free, t0_top, tier, slot, s, rl_loc, rl_pos, rl_count, Nmax,
-                                      S0, N, n);
-    open_commit_kernel<<<1, 32 * ((B + 31) / 32), 0, st>>>(t0_top, rl_count, B, n);
+    const int fused = n <= 256;
+    open_kernel<<<grid, 256, 0, st>>>(t0_free, t0_top, tier, slot, s, rl_loc, rl_pos, rl_count, pos_n, Nmax,
+                                      S0, n, fused);
+    *launches = 1;
+    if (!fused) {
+        open_commit_kernel<<<1, 32 * ((B + 31) / 32), 0, st>>>(t0_top, rl_count, pos_n, B, n);
+        *launches = 2;
+    }
     return cudaGetLastError();
 }
 

@@ -48,6 +48,7 @@ struct tkv_ctx {
     RetierOut* outp = nullptr;
     RetierParams* params = nullptr;
     int32_t* err = nullptr;
+    int32_t* pos_n = nullptr;                // [B] committed positions (device copy of N)
 
     // pinned host
     __nv_bfloat16 *h1 = nullptr, *h2m = nullptr;      // host pointers
@@ -70,6 +71,23 @@ struct tkv_ctx {
     std::vector<char> prefetched;
     // decode-token rows appended but not yet written (the layer's attention kernel writes them)
     std::vector<const void*> pend_k, pend_v;
+
+    // CUDA-graph decode steps
+    bool capturing = false;
+    cudaStream_t cap_stream = nullptr, cap_saved_compute = nullptr;
+    cudaEvent_t ev_fork = nullptr;        // recorded on the capture stream when the capture opens
+    bool copy_joined = false;             // the copy stream has joined the capture
+    bool attn_in_capture[2] = {false, false};
+    int cap_rows = 0;                     // rows per group the captured launch geometry covers
+    struct Saved {
+        int N;
+        std::vector<int> count0, R;
+        int64_t step, launches;
+        tkv_stats st;
+    } cap_saved;
+    cudaGraphExec_t graph_exec = nullptr;
+    int graph_steps_left = 0;
+    int64_t graph_launches = 0, graph_t1_bytes = 0;
     int delta_max = 0;                 // pending delta moves (max over sequences), 0 = none
 
     int resident = 1;                  // attention CTAs resident on the device at once
@@ -161,7 +179,7 @@ void free_all(tkv_ctx* c) {
     cudaFree(c->s); cudaFree(c->rl_loc); cudaFree(c->rl_pos); cudaFree(c->rl_count);
     cudaFree(c->g); cudaFree(c->part); cudaFree(c->zs); cudaFree(c->t0_free); cudaFree(c->t0_top);
     cudaFree(c->moves_now); cudaFree(c->moves_delta); cudaFree(c->outp); cudaFree(c->params);
-    cudaFree(c->err);
+    cudaFree(c->err); cudaFree(c->pos_n);
     cudaFreeHost(c->h1); cudaFreeHost(c->h2m); cudaFreeHost(c->h_outp); cudaFreeHost(c->h_params);
     cudaFreeHost(c->h_err);
     for (int i = 0; i < 2; ++i) {
@@ -169,6 +187,9 @@ void free_all(tkv_ctx* c) {
         if (c->ev_attn[i]) cudaEventDestroy(c->ev_attn[i]);
     }
     if (c->ev_retier) cudaEventDestroy(c->ev_retier);
+    if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     for (auto& v : c->prof_ev)
         for (cudaEvent_t e : v) cudaEventDestroy(e);
     if (c->own_compute && c->compute) cudaStreamDestroy(c->compute);
@@ -204,6 +225,25 @@ tkv_status read_device_status(tkv_ctx* ctx) {
 }
 
 // Enqueues the delta moves left by the last re-tier for layers [l0, l1).
+// Events recorded inside a capture only mark points of that capture, and a replay does
+// not record them.  After a capture and after every replay they are recorded again on
+// the compute stream, behind everything the replay did (copy-stream work included), so
+// the eager calls that follow wait on the right work.
+cudaError_t rerecord_events(tkv_ctx* ctx) {
+    for (int i = 0; i < 2; ++i) {
+        cudaError_t e = cudaEventRecord(ctx->ev_attn[i], ctx->compute);
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_t1[i], ctx->compute);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+void drop_graph(tkv_ctx* ctx) {
+    if (ctx->graph_exec) cudaGraphExecDestroy(ctx->graph_exec);
+    ctx->graph_exec = nullptr;
+    ctx->graph_steps_left = 0;
+}
+
 tkv_status enqueue_delta(tkv_ctx* ctx, int l0, int l1, cudaStream_t st) {
     if (ctx->delta_max <= 0) return TKV_OK;
     MoveArgs m{};
@@ -229,6 +269,7 @@ tkv_status enqueue_delta(tkv_ctx* ctx, int l0, int l1, cudaStream_t st) {
 // Re-tier core shared by tkv_retier (ranked) and tkv_set_tiers (forced).
 tkv_status run_retier(tkv_ctx* ctx, bool forced) {
     const int N = ctx->N, B = ctx->B;
+    drop_graph(ctx);
     // a delta left by an earlier re-tier that no decode step has consumed yet
     if (ctx->delta_max > 0) {
         tkv_status r = enqueue_delta(ctx, 0, ctx->L, ctx->compute);
@@ -314,8 +355,18 @@ tkv_status run_retier(tkv_ctx* ctx, bool forced) {
 
 tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
     const int slotr = layer & 1;
-    CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_attn[slotr], 0));
-    CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_retier, 0));
+    if (ctx->capturing) {
+        // Inside a captured step only events recorded in the capture order the copy
+        // stream; a replay as a whole follows everything enqueued before it.
+        if (!ctx->copy_joined) {
+            CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_fork, 0));
+            ctx->copy_joined = true;
+        }
+        if (ctx->attn_in_capture[slotr]) CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_attn[slotr], 0));
+    } else {
+        CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_attn[slotr], 0));
+        CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_retier, 0));
+    }
     if (ctx->hw1 > 0) {
         const size_t pitch = (size_t)ctx->S1 * ctx->d * sizeof(__nv_bfloat16);
         const size_t layer_elems = (size_t)2 * ctx->B * ctx->Hkv * ctx->S1 * ctx->d;
@@ -481,6 +532,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     A(dalloc(ctx, &ctx->outp, B));
     A(dalloc(ctx, &ctx->params, B));
     A(dalloc(ctx, &ctx->err, 1));
+    A(dalloc(ctx, &ctx->pos_n, B));
     if (!ok) {
         (void)cudaGetLastError();
         return bail(TKV_ENOMEM);
@@ -514,11 +566,14 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     E(cudaMemset(ctx->s, 0, B * Nmax * 4));
     E(cudaMemset(ctx->outp, 0, B * sizeof(RetierOut)));
     E(cudaMemset(ctx->err, 0, 4));
+    E(cudaMemset(ctx->pos_n, 0, B * 4));
     for (int i = 0; i < 2; ++i) {
         E(cudaEventCreateWithFlags(&ctx->ev_t1[i], cudaEventDisableTiming));
         E(cudaEventCreateWithFlags(&ctx->ev_attn[i], cudaEventDisableTiming));
     }
     E(cudaEventCreateWithFlags(&ctx->ev_retier, cudaEventDisableTiming));
+    E(cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming));
+    E(cudaStreamCreateWithFlags(&ctx->cap_stream, cudaStreamNonBlocking));
     E(cudaEventCreateWithFlags(&ctx->ev_split, cudaEventDisableTiming));
     E(cudaStreamCreateWithFlags(&ctx->copy2, cudaStreamNonBlocking));
     for (int i = 0; i < tkv_ctx::kCopyLanes - 1; ++i) {
@@ -556,6 +611,14 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
 void tkv_destroy(tkv_ctx* ctx) {
     if (!ctx) return;
     DeviceGuard guard(ctx->device);
+    if (ctx->capturing) {
+        cudaGraph_t g = nullptr;
+        cudaStreamEndCapture(ctx->cap_stream, &g);
+        if (g) cudaGraphDestroy(g);
+        ctx->compute = ctx->cap_saved_compute;
+        ctx->capturing = false;
+        (void)cudaGetLastError();
+    }
     if (ctx->compute) cudaStreamSynchronize(ctx->compute);
     if (ctx->copy) cudaStreamSynchronize(ctx->copy);
     free_all(ctx);
@@ -565,16 +628,19 @@ void tkv_destroy(tkv_ctx* ctx) {
 tkv_status tkv_append(tkv_ctx* ctx, int32_t layer, const void* k, const void* v, int32_t n_tokens) {
     CHECK_CTX();
     if (!k || !v || n_tokens < 1 || layer < 0 || layer >= ctx->L) return TKV_EINVAL;
+    if (n_tokens > 1 && ctx->capturing) return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
+    if (n_tokens > 1) drop_graph(ctx);
     const int B = ctx->B;
     if (ctx->open_n == 0) {
         if (layer != 0) return TKV_EINVAL;
         if (ctx->N + n_tokens > ctx->Nmax) return TKV_ECAPACITY;
         for (int b = 0; b < B; ++b)
             if (ctx->count[0][b] + n_tokens > ctx->S0) return TKV_ECAPACITY;
+        int nl = 0;
         CK(launch_open(ctx->t0_free, ctx->t0_top, ctx->tier, ctx->slot, ctx->s, ctx->rl_loc, ctx->rl_pos,
-                       ctx->rl_count, B, ctx->Nmax, ctx->S0, ctx->N, n_tokens, ctx->compute));
-        ctx->launches += 2;
+                       ctx->rl_count, ctx->pos_n, B, ctx->Nmax, ctx->S0, n_tokens, ctx->compute, &nl));
+        ctx->launches += nl;
         for (int b = 0; b < B; ++b) {
             ctx->count[0][b] += n_tokens;
             ctx->R[b] += n_tokens;
@@ -662,11 +728,17 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
         prof_close(ctx, 0, ctx->compute, bytes);
     }
     CK(cudaEventRecord(ctx->ev_attn[slotr], ctx->compute));
+    if (ctx->capturing) {
+        ctx->attn_in_capture[slotr] = true;
+        ctx->cap_rows = plan.items_per_group * plan.item_rows;
+    }
     ctx->last_splits = plan.grid;
     ctx->decoded++;
     if (ctx->decoded == ctx->L) {
         const float inv = (float)(1.0 / ((double)ctx->L * (double)ctx->Hq));
-        CK(launch_fold(ctx->g, ctx->rl_pos, ctx->rl_count, ctx->s, ctx->B, ctx->Hkv, ctx->Nmax, rmax,
+        // a captured fold covers every retained count its replays can meet
+        CK(launch_fold(ctx->g, ctx->rl_pos, ctx->rl_count, ctx->s, ctx->B, ctx->Hkv, ctx->Nmax,
+                       ctx->capturing ? ctx->cap_rows : rmax,
                        inv, ctx->compute));
         ctx->launches++;
         ctx->N += 1;
@@ -679,13 +751,14 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
 
 tkv_status tkv_retier(tkv_ctx* ctx) {
     CHECK_CTX();
-    if (ctx->open_n != 0) return TKV_EINVAL;
+    if (ctx->open_n != 0 || ctx->capturing) return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
     return run_retier(ctx, false);
 }
 
 tkv_status tkv_get_scores(tkv_ctx* ctx, float* dst) {
     CHECK_CTX();
+    if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     if (!dst) return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
     CK(cudaStreamSynchronize(ctx->copy));
@@ -698,6 +771,7 @@ tkv_status tkv_get_scores(tkv_ctx* ctx, float* dst) {
 
 tkv_status tkv_set_scores(tkv_ctx* ctx, const float* src) {
     CHECK_CTX();
+    if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     if (!src || ctx->open_n != 0) return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
     CK(cudaStreamSynchronize(ctx->compute));
@@ -709,6 +783,7 @@ tkv_status tkv_set_scores(tkv_ctx* ctx, const float* src) {
 
 tkv_status tkv_get_tiers(tkv_ctx* ctx, uint8_t* dst) {
     CHECK_CTX();
+    if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     if (!dst) return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
     CK(cudaStreamSynchronize(ctx->copy));
@@ -720,6 +795,7 @@ tkv_status tkv_get_tiers(tkv_ctx* ctx, uint8_t* dst) {
 
 tkv_status tkv_set_tiers(tkv_ctx* ctx, const uint8_t* src) {
     CHECK_CTX();
+    if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     if (!src || ctx->open_n != 0) return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
     const int N = ctx->N, B = ctx->B;
@@ -738,6 +814,7 @@ tkv_status tkv_set_tiers(tkv_ctx* ctx, const uint8_t* src) {
 tkv_status tkv_get_row(tkv_ctx* ctx, int32_t layer, int32_t seq, int32_t pos, void* dst,
                        float* scales, int32_t* tier_out) {
     CHECK_CTX();
+    if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     if (!dst || !tier_out || layer < 0 || layer >= ctx->L || seq < 0 || seq >= ctx->B || pos < 0 ||
         pos >= ctx->N)
         return TKV_EINVAL;
@@ -774,6 +851,7 @@ tkv_status tkv_get_row(tkv_ctx* ctx, int32_t layer, int32_t seq, int32_t pos, vo
 
 tkv_status tkv_profile_begin(tkv_ctx* ctx) {
     CHECK_CTX();
+    if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     DeviceGuard guard(ctx->device);
     for (int k = 0; k < 3; ++k) {
         if (ctx->prof_ev[k].empty()) {
@@ -789,6 +867,7 @@ tkv_status tkv_profile_begin(tkv_ctx* ctx) {
 
 tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t1, tkv_prof_entry* delta) {
     CHECK_CTX();
+    if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     DeviceGuard guard(ctx->device);
     ctx->profiling = false;
     CK(cudaStreamSynchronize(ctx->copy));
@@ -810,8 +889,114 @@ tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t
     return read_device_status(ctx);
 }
 
+tkv_status tkv_capture_begin(tkv_ctx* ctx) {
+    CHECK_CTX();
+    if (ctx->capturing || ctx->open_n != 0 || ctx->delta_max > 0 || ctx->profiling) return TKV_EINVAL;
+    if (ctx->cfg.t1_transport != TKV_T1_COPY_ENGINE && ctx->cfg.t1_transport != TKV_T1_SM_COPY) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    drop_graph(ctx);
+    ctx->cap_saved.N = ctx->N;
+    ctx->cap_saved.count0 = ctx->count[0];
+    ctx->cap_saved.R = ctx->R;
+    ctx->cap_saved.step = ctx->step;
+    ctx->cap_saved.launches = ctx->launches;
+    ctx->cap_saved.st = ctx->st;
+    CK(cudaStreamBeginCapture(ctx->cap_stream, cudaStreamCaptureModeThreadLocal));
+    if (cudaEventRecord(ctx->ev_fork, ctx->cap_stream) != cudaSuccess) {
+        cudaGraph_t g = nullptr;
+        cudaStreamEndCapture(ctx->cap_stream, &g);
+        if (g) cudaGraphDestroy(g);
+        (void)cudaGetLastError();
+        return fail(ctx, TKV_ECUDA);
+    }
+    ctx->cap_saved_compute = ctx->compute;
+    ctx->compute = ctx->cap_stream;
+    ctx->capturing = true;
+    ctx->copy_joined = false;
+    ctx->attn_in_capture[0] = ctx->attn_in_capture[1] = false;
+    ctx->cap_rows = 0;
+    return TKV_OK;
+}
+
+tkv_status tkv_capture_end(tkv_ctx* ctx, int32_t* steps_valid) {
+    if (!ctx || !ctx->capturing) return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(ctx->cap_stream, &graph);
+    ctx->capturing = false;
+    ctx->compute = ctx->cap_saved_compute;
+    const bool one_step = ctx->open_n == 0 && ctx->step == ctx->cap_saved.step + 1;
+    const int64_t launches = ctx->launches - ctx->cap_saved.launches;
+    const int64_t t1 = ctx->st.h2d_bytes_t1_stream - ctx->cap_saved.st.h2d_bytes_t1_stream;
+    // nothing of the captured step has run: back to the state before it
+    ctx->N = ctx->cap_saved.N;
+    ctx->count[0] = ctx->cap_saved.count0;
+    ctx->R = ctx->cap_saved.R;
+    ctx->step = ctx->cap_saved.step;
+    ctx->launches = ctx->cap_saved.launches;
+    ctx->st = ctx->cap_saved.st;
+    ctx->open_n = 0;
+    ctx->appended = ctx->decoded = 0;
+    std::fill(ctx->pend_k.begin(), ctx->pend_k.end(), nullptr);
+    std::fill(ctx->pend_v.begin(), ctx->pend_v.end(), nullptr);
+    if (rerecord_events(ctx) != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        (void)cudaGetLastError();
+        return fail(ctx, TKV_ECUDA);
+    }
+    if (ce != cudaSuccess || !graph) {
+        (void)cudaGetLastError();
+        return fail(ctx, TKV_ECUDA);
+    }
+    if (!one_step) {
+        cudaGraphDestroy(graph);
+        return TKV_EINVAL;
+    }
+    const cudaError_t ie = cudaGraphInstantiate(&ctx->graph_exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) {
+        ctx->graph_exec = nullptr;
+        (void)cudaGetLastError();
+        return fail(ctx, TKV_ECUDA);
+    }
+    // replay k (from 1) decodes with R_b + k retained rows and N + k positions
+    int rmax = 0, c0max = 0;
+    for (int b = 0; b < ctx->B; ++b) {
+        rmax = std::max(rmax, ctx->R[b]);
+        c0max = std::max(c0max, ctx->count[0][b]);
+    }
+    int valid = std::min(ctx->cap_rows - rmax, ctx->Nmax - ctx->N);
+    valid = std::max(0, std::min(valid, ctx->S0 - c0max));
+    ctx->graph_steps_left = valid;
+    ctx->graph_launches = launches;
+    ctx->graph_t1_bytes = t1;
+    if (steps_valid) *steps_valid = valid;
+    return TKV_OK;
+}
+
+tkv_status tkv_replay(tkv_ctx* ctx) {
+    CHECK_CTX();
+    if (ctx->capturing || !ctx->graph_exec || ctx->graph_steps_left <= 0 || ctx->open_n != 0 ||
+        ctx->delta_max > 0)
+        return TKV_EINVAL;
+    DeviceGuard guard(ctx->device);
+    CK(cudaGraphLaunch(ctx->graph_exec, ctx->compute));
+    CK(rerecord_events(ctx));
+    ctx->N += 1;
+    for (int b = 0; b < ctx->B; ++b) {
+        ctx->count[0][b] += 1;
+        ctx->R[b] += 1;
+    }
+    ctx->step++;
+    ctx->launches += ctx->graph_launches;
+    ctx->st.h2d_bytes_t1_stream += ctx->graph_t1_bytes;
+    ctx->graph_steps_left--;
+    return TKV_OK;
+}
+
 tkv_status tkv_sync(tkv_ctx* ctx) {
     CHECK_CTX();
+    if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     DeviceGuard guard(ctx->device);
     CK(cudaStreamSynchronize(ctx->copy));
     CK(cudaStreamSynchronize(ctx->compute));

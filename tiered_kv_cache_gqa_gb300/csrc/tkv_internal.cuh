@@ -195,8 +195,8 @@ cudaError_t launch_fold(const float* g, const int32_t* rl_pos, const int32_t* rl
                         int B, int Hkv, int Nmax, int rmax, float inv_lh, cudaStream_t st);
 
 cudaError_t launch_open(int32_t* t0_free, int32_t* t0_top, uint8_t* tier, int32_t* slot, float* s,
-                        uint32_t* rl_loc, int32_t* rl_pos, int32_t* rl_count, int B, int Nmax,
-                        int S0, int N, int n, cudaStream_t st);
+                        uint32_t* rl_loc, int32_t* rl_pos, int32_t* rl_count, int32_t* pos_n, int B, int Nmax,
+                        int S0, int n, cudaStream_t st, int* launches);
 
 cudaError_t launch_append_rows(const __nv_bfloat16* k, const __nv_bfloat16* v,
                                __nv_bfloat16* k0v0, const int32_t* slot, int layer, int B,
