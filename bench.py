@@ -31,7 +31,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "tiered decode-attn tokens/s (HBM GB/s vs peak); delta-prefetch PCIe GB/s"
-PRE_STEPS = 64            # decode steps before the first re-tier (scores accumulate)
+# Decode steps before the profiled pass: two re-tiers (after steps 64 and 128).  The first
+# only demotes (every token starts in T0); the second also promotes, so the profiled
+# pass that follows it carries a delta prefetch.
+PRE_STEPS = 128
 TARGET_N = {"tiny": 640, "7b": 2512, "14b": 4096, "32b": 8192, "70b": 16384}
 DESCR = {
     "tiny": "Tiny: 1 layer, 4/2 heads, d 64, batch 1",
@@ -58,6 +61,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-exposed", action="store_true",
+                   help="skip the all-T0 run that measures the exposed transfer overhead")
     p.add_argument("--mode", choices=["graph", "eager"], default="graph",
                    help="timed steps: replays of a captured decode step, or eager per-layer calls")
     p.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
@@ -291,81 +296,102 @@ def run_gpu(args, rank, world):
                 self.c.retier()
                 self.left = 0
 
+    # Timeline (positions are the same in every loop below):
+    #   steps 1..128 eager, re-tiers after steps 64 and 128;
+    #   KP eager profiled steps (the first carries the delta prefetch of that re-tier);
+    #   W warm-up steps and K timed steps, replayed (or eager with --mode eager).
+    def lead_in(c, r, profile):
+        t = 0
+        for _ in range(PRE_STEPS):
+            t += 1
+            r(t, *inputs[t - 1], False)
+        prof, prof_ms = None, 0.0
+        if profile:
+            c.profile_begin()
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KP)]
+        for i in range(KP):
+            t += 1
+            flush.fill_(i & 0xFF)
+            pev[i][0].record(stream)
+            r(t, *inputs[t - 1], False)
+            pev[i][1].record(stream)
+        if profile:
+            prof = c.profile_end()
+        torch.cuda.synchronize()
+        prof_ms = sum(x.elapsed_time(y) for x, y in pev)
+        for _ in range(args.warmup):
+            t += 1
+            r(t, *inputs[t - 1], graph)
+        c.sync()
+        torch.cuda.synchronize()
+        return t, prof, prof_ms
+
+    def timed(c, r, t, sample_clocks):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        sampler = ClockSampler(dev) if (rank == 0 and sample_clocks) else None
+        if sampler:
+            sampler.start()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        launches0 = c.stats()["kernel_launches"]
+        captures0 = r.captures
+        # marks the timed region for a profiler started with collection off (no-op otherwise)
+        if sample_clocks:
+            torch.cuda.profiler.start()
+        for i in range(args.steps):
+            t += 1
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            r(t, *inputs[t - 1], graph)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if sample_clocks:
+            torch.cuda.profiler.stop()
+        if world > 1:
+            torch.distributed.barrier()
+        clocks = sampler.stop() if sampler else None
+        step_ms = [x.elapsed_time(y) for x, y in ev]
+        return (t, step_ms, clocks, c.stats()["kernel_launches"] - launches0, r.captures - captures0)
+
     ctx = new_context()
     run = Stepper(ctx)
-    t = 0
-    for _ in range(PRE_STEPS):
-        t += 1
-        run(t, *inputs[t - 1], False)
-    for _ in range(args.warmup):
-        t += 1
-        run(t, *inputs[t - 1], graph)
-    ctx.sync()
-    torch.cuda.synchronize()
-
-    # ---- timed: inputs resident in HBM, L2 flushed between steps
-    launches0 = ctx.stats()["kernel_launches"]
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    sampler = ClockSampler(dev) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    # marks the timed region for a profiler started with collection off (no-op otherwise)
-    torch.cuda.profiler.start()
-    captures0 = run.captures
-    for i in range(args.steps):
-        t += 1
-        flush.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        run(t, *inputs[t - 1], graph)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    torch.cuda.profiler.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop() if sampler else None
-    step_ms = [a.elapsed_time(b) for a, b in ev]
+    t, prof, prof_ms = lead_in(ctx, run, True)
+    t_first = t + 1
+    t, step_ms, clocks, launches, captures = timed(ctx, run, t, True)
     total_ms = sum(step_ms)
-    launches = ctx.stats()["kernel_launches"] - launches0
-    captures = run.captures - captures0
-
-    # ---- profiled pass: the same decode, eager, with events around every attention launch
-    ctx.profile_begin()
-    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KP)]
-    for i in range(KP):
-        t += 1
-        flush.fill_(i & 0xFF)
-        pev[i][0].record(stream)
-        run(t, *inputs[t - 1], False)
-        pev[i][1].record(stream)
-    prof = ctx.profile_end()
-    torch.cuda.synchronize()
-    prof_ms = sum(a.elapsed_time(b) for a, b in pev)
     st = ctx.stats()
+    ctx.close()
+
+    # ---- exposed transfer overhead: the same timeline with every retained row in T0
+    exposed = None
+    if not args.no_exposed:
+        r = list(wl.ratios)
+        wl_t0 = wl.with_(ratios=(1.0 - r[3], 0.0, 0.0, r[3]))
+        c0 = tkv.TieredKV.for_workload(wl_t0, device=dev, t1_transport=t1_mode)
+        for l in range(L):
+            K, V = gen.prefill_layer(l)
+            c0.append(l, K, V, wl.prefill_len)
+            del K, V
+        r0 = Stepper(c0)
+        t0_, _, _ = lead_in(c0, r0, False)
+        _, step_ms0, _, _, _ = timed(c0, r0, t0_, False)
+        c0.close()
+        exposed = {"all_t0_ms_per_step": sum(step_ms0) / args.steps,
+                   "share": (total_ms - sum(step_ms0)) / total_ms}
 
     # ---- e2e: the same steps fed from pinned host buffers, outputs copied back
     e2e = None
     if not args.no_e2e:
-        t_first = PRE_STEPS + args.warmup + 1
         host_in = [(q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory())
                    for (q, k, v) in inputs[t_first - 1: t_first - 1 + args.steps]]
         dq, dk, dv = (torch.empty_like(x) for x in inputs[0])
         host_out = torch.empty(L, B, Hq, d, dtype=torch.float32).pin_memory()
-        # replay the same decode positions on a fresh context so both loops see the same state
-        ctx.close()
+        # the same decode positions on a fresh context, so both loops see the same state
         ctx = new_context()
         run = Stepper(ctx)
-        t = 0
-        for _ in range(PRE_STEPS):
-            t += 1
-            run(t, *inputs[t - 1], False)
-        for _ in range(args.warmup):
-            t += 1
-            run(t, *inputs[t - 1], graph)
-        torch.cuda.synchronize()
+        t, _, _ = lead_in(ctx, run, False)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             torch.distributed.barrier()
@@ -384,10 +410,10 @@ def run_gpu(args, rank, world):
         h2d = sum(x.numel() * x.element_size() for x in host_in[0])
         d2h = host_out.numel() * host_out.element_size()
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
-    ctx.close()
+        ctx.close()
     return {"total_ms": total_ms, "step_ms": step_ms, "prof": prof, "stats": st, "clocks": clocks,
             "launches": launches, "wl": wl, "e2e": e2e, "captures": captures, "prof_steps": KP,
-            "prof_ms": prof_ms}
+            "prof_ms": prof_ms, "exposed": exposed}
 
 
 def main():
@@ -480,6 +506,7 @@ def main():
             "delta_prefetch": {"gbs": delta_gbs, "bytes": pd["bytes"], "ms": pd["ms"]},
             "link_peak_gbs_nominal_pcie5x16": 64.0,
             "transfer_overhead_copy_share": link_ms / r["prof_ms"],
+            "transfer_overhead_exposed": r["exposed"],
             "hbm_saved_bytes": st["kv_bytes_full_cache"] - st["hbm_bytes_kv_resident"],
             "hbm_kv_resident_bytes": st["hbm_bytes_kv_resident"],
             "kv_full_cache_bytes": st["kv_bytes_full_cache"],
