@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     const uint8_t* row_v = nullptr;    // the lane's V row of the tile whose K was issued last
     int row_bytes = 0;
     uint32_t fp8_mask_issue = 0;       // T2 rows of the tile last issued as K
+    bool all_bf16_issue = false;       // that tile has 32 bf16 rows (its K and V copies take the fast path)
     // Copies the next tile of this warp's sequence: 16 lanes per 256-byte row, 16 bytes
     // a lane; a row's source pointer travels by shuffle with its kind in the low bits
     // (bit 0: T2 record of D + 16 bytes, bit 1: no row).
@@ -200,17 +201,29 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         } else {
             src = row_v;
         }
-        const unsigned long long tagged = (unsigned long long)src | (row_bytes == D + 16 ? 1ull : 0ull) |
-                                          (row_bytes ? 0ull : 2ull);
+        if (kv == 0) all_bf16_issue = __all_sync(0xffffffffu, row_bytes == 2 * D);
         const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * C::sz_stage);
         const int col = lane & 15, half = lane >> 4;
+        if (all_bf16_issue) {
+            // 32 bf16 rows: no per-row kinds to decode
+#pragma unroll 8
+            for (int rr = 0; rr < kRows / 2; ++rr) {
+                const int r = 2 * rr + half;
+                const uint8_t* rsrc = reinterpret_cast<const uint8_t*>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), r));
+                if (col * 16 < 2 * D) cp_async16(dst0 + r * ROWB + col * 16, rsrc + col * 16);
+            }
+        } else {
+            const unsigned long long tagged = (unsigned long long)src | (row_bytes == D + 16 ? 1ull : 0ull) |
+                                              (row_bytes ? 0ull : 2ull);
 #pragma unroll 4
-        for (int rr = 0; rr < kRows / 2; ++rr) {
-            const int r = 2 * rr + half;
-            const unsigned long long t = __shfl_sync(0xffffffffu, tagged, r);
-            const uint8_t* rsrc = (const uint8_t*)(t & ~15ull);
-            const int nb = (t & 2ull) ? 0 : ((t & 1ull) ? D + 16 : 2 * D);
-            if (col * 16 < nb) cp_async16(dst0 + r * ROWB + col * 16, rsrc + col * 16);
+            for (int rr = 0; rr < kRows / 2; ++rr) {
+                const int r = 2 * rr + half;
+                const unsigned long long t = __shfl_sync(0xffffffffu, tagged, r);
+                const uint8_t* rsrc = (const uint8_t*)(t & ~15ull);
+                const int nb = (t & 2ull) ? 0 : ((t & 1ull) ? D + 16 : 2 * D);
+                if (col * 16 < nb) cp_async16(dst0 + r * ROWB + col * 16, rsrc + col * 16);
+            }
         }
         ++issued;
         if (ci_kv == 0) {
@@ -332,12 +345,27 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
 #pragma unroll
                 for (int h = 0; h < G; ++h) acc[h] = acc2[h] = make_float2(0.f, 0.f);
                 float zscale = 1.0f;
-                if (!((tmask >> lane) & 1u)) {
-#pragma unroll
+                if (tmask != 0u) {
+                    // a tile with T2 rows: lanes load and convert their own kind of row, the
+                    // FMAs are shared (no serialised second pass over the chunk loop)
+                    const bool f8 = (tmask >> lane) & 1u;
+                    if (f8) zscale = *reinterpret_cast<const float*>(row + D);
+#pragma unroll 4
                     for (int c = 0; c < D / 8; ++c) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
-                        const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
-                        const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+                        float2 k0, k1, k2, k3;
+                        if (!f8) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
+                            k0 = bf16x2_to_float2(w.x);
+                            k1 = bf16x2_to_float2(w.y);
+                            k2 = bf16x2_to_float2(w.z);
+                            k3 = bf16x2_to_float2(w.w);
+                        } else {
+                            const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
+                            k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
+                            k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
+                            k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
+                            k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
+                        }
 #pragma unroll
                         for (int h = 0; h < G; ++h) {
                             const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
@@ -349,14 +377,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                         }
                     }
                 } else {
-                    zscale = *reinterpret_cast<const float*>(row + D);
-#pragma unroll 4
+#pragma unroll
                     for (int c = 0; c < D / 8; ++c) {
-                        const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
-                        const float2 k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
-                        const float2 k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
-                        const float2 k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
-                        const float2 k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
+                        const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
+                        const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+                        const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
 #pragma unroll
                         for (int h = 0; h < G; ++h) {
                             const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
@@ -456,6 +481,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
 #pragma unroll
                     for (int r = 0; r < kRows; ++r) pv_row(r, false);
                 } else {
+#pragma unroll 4
                     for (int r = 0; r < nrows; ++r) pv_row(r, (tmask >> r) & 1u);
                 }
             }
