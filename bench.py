@@ -94,6 +94,24 @@ def describe(wl):
                *(100 * x for x in wl.ratios), wl.num_sinks, wl.window))
 
 
+def ncu_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary of this workload's
+    attention kernel, if it was captured from the attention source as it is now; else None.
+    The summary holds a line `traffic: <workload> <bytes per launch> <sha256 of attention.cu>`."""
+    import hashlib
+    src = os.path.join(ROOT, "tiered_kv_cache_gqa_gb300", "csrc", "attention.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
+            for line in open(os.path.join(ROOT, "profiles", name)):
+                f = line.strip().strip("`").split()
+                if len(f) == 4 and f[0] == "traffic:" and f[1] == workload and f[3] == digest:
+                    return float(f[2])
+    except OSError:
+        return None
+    return None
+
+
 def synth_layers(name):
     from tiered_kv_cache_gqa_gb300 import synth
     return synth.WORKLOADS[name].num_layers
@@ -487,7 +505,7 @@ def main():
                    "l2": "flushed between timed steps (256 MB write); step working set %.0f MB"
                          % (st["kv_bytes_full_cache"] / 2 ** 20)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": ncu_traffic(args.workload) if not args.layers else None,
                      "kernel": "tkv::attn_kernel", "peak_source": peak_src,
                      "launches": pa["count"], "avg_launch_us": 1e3 * pa["ms"] / max(1, pa["count"]),
                      "bytes_per_launch": pa["bytes"] / max(1, pa["count"])},

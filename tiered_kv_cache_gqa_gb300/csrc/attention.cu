@@ -74,10 +74,16 @@ __device__ __forceinline__ void cp_async_wait_prev() {
     asm volatile("cp.async.wait_group %0;" ::"n"(kWarpStages - 1) : "memory");
 }
 
-template <int G, int D>
+// COMPACT: partly unrolled loops, for launches in which every warp streams one or two
+// tiles: the code then runs about once per launch and the instruction cache, not the
+// arithmetic, sets its pace.
+template <int G, int D, bool COMPACT>
 __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
     constexpr int GP = C::GP, ROWB = C::ROWB, CPL = C::CPL, PS = C::PS;
+    constexpr int kQKUnroll = COMPACT ? 4 : D / 8;      // chunks of 8 elements of a K row
+    constexpr int kPVUnroll = COMPACT ? 4 : kRows;      // rows of a V tile
+    constexpr int kIssueUnroll = COMPACT ? 4 : 8;
     constexpr int NT = kAttnWarps * 32;
     extern __shared__ __align__(128) uint8_t smem[];
     float* q_s = reinterpret_cast<float*>(smem + C::off_q);
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         const int col = lane & 15, half = lane >> 4;
         if (all_bf16_issue) {
             // 32 bf16 rows: no per-row kinds to decode
-#pragma unroll 8
+#pragma unroll kIssueUnroll
             for (int rr = 0; rr < kRows / 2; ++rr) {
                 const int r = 2 * rr + half;
                 const uint8_t* rsrc = reinterpret_cast<const uint8_t*>(
@@ -377,7 +383,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                         }
                     }
                 } else {
-#pragma unroll
+#pragma unroll kQKUnroll
                     for (int c = 0; c < D / 8; ++c) {
                         const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
                         const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
@@ -478,7 +484,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                         for (int c = 0; c < CPL / 2; ++c) o[h][c] = __ffma2_rn(pp[h], v[c], o[h][c]);
                 };
                 if (nrows == kRows && tmask == 0u) {
-#pragma unroll
+#pragma unroll kPVUnroll
                     for (int r = 0; r < kRows; ++r) pv_row(r, false);
                 } else {
 #pragma unroll 4
@@ -550,22 +556,32 @@ __global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) 
     float* gj = a.g + ((size_t)b * a.Hkv + kvh) * a.Nmax + j;
     const float g_prev = (has_row && a.layer > 0) ? *gj : 0.f;
     __syncthreads();
-    // (2) the group's M and L per head, and every segment's factor 2^(m - M) / L
-    if (threadIdx.x < G) {
-        const int h = threadIdx.x;
-        float M = -INFINITY;
-        for (int sg = 0; sg < ns; ++sg) M = fmaxf(M, m_s[sg * 8 + h]);
-        float L = 0.f;
-        for (int sg = 0; sg < ns; ++sg) {
-            const float ms = m_s[sg * 8 + h];
-            const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-            f_s[sg * 8 + h] = f;
-            L += f * l_s[sg * 8 + h];
+    // (2) the group's M and L per head (one warp per head, segments across lanes, fixed
+    // shuffle order), and every segment's factor 2^(m - M) / L
+    {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (w < G) {
+            const int h = w;
+            float M = -INFINITY;
+            for (int sg = lane; sg < ns; sg += 32) M = fmaxf(M, m_s[sg * 8 + h]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float L = 0.f;
+            for (int sg = lane; sg < ns; sg += 32) {
+                const float ms = m_s[sg * 8 + h];
+                const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+                f_s[sg * 8 + h] = f;
+                L += f * l_s[sg * 8 + h];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            const float inv = 1.0f / L;
+            for (int sg = lane; sg < ns; sg += 32) f_s[sg * 8 + h] *= inv;
+            if (lane == 0) {
+                Ms[h] = M;
+                Linv[h] = inv;
+            }
         }
-        const float inv = 1.0f / L;
-        for (int sg = 0; sg < ns; ++sg) f_s[sg * 8 + h] *= inv;
-        Ms[h] = M;
-        Linv[h] = inv;
     }
     __syncthreads();
     // (3) out, summed in segment order; groups with more than kSegBatch segments load the rest now
@@ -598,7 +614,11 @@ template <int G, int D>
 static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
     using C = AttnCfg<G, D>;
     const size_t smem = C::smem(a.items_per_cta * a.item_rows);
-    attn_kernel<G, D><<<a.grid, kAttnWarps * 32, smem, st>>>(a);
+    // at most two tiles per warp: the compact instantiation
+    if (a.items_per_cta * a.item_rows <= 2 * kRows * kAttnWarps)
+        attn_kernel<G, D, true><<<a.grid, kAttnWarps * 32, smem, st>>>(a);
+    else
+        attn_kernel<G, D, false><<<a.grid, kAttnWarps * 32, smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // one alpha row per thread; enough blocks that every block holds at most 256 out elements
@@ -625,7 +645,9 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
 
 template <int G, int D>
 static cudaError_t prepare_gd(size_t smem) {
-    return cudaFuncSetAttribute(attn_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<G, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(attn_kernel<G, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
 template <int G, int D>
@@ -636,7 +658,7 @@ static size_t smem_gd(int rl_rows) {
 template <int G, int D>
 static int resident_gd(size_t smem) {
     int per_sm = 0, dev = 0, sms = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_kernel<G, D>, kAttnWarps * 32, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_kernel<G, D, false>, kAttnWarps * 32, smem) != cudaSuccess ||
         cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
@@ -647,9 +669,13 @@ static int resident_gd(size_t smem) {
 template <int G, int D>
 static cudaError_t ensure_smem_gd(size_t smem) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_kernel<G, D>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_kernel<G, D, false>);
     if (e != cudaSuccess) return e;
-    if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
+    cudaFuncAttributes fc;
+    e = cudaFuncGetAttributes(&fc, attn_kernel<G, D, true>);
+    if (e != cudaSuccess) return e;
+    if ((size_t)fa.maxDynamicSharedSizeBytes >= smem && (size_t)fc.maxDynamicSharedSizeBytes >= smem)
+        return cudaSuccess;
     return prepare_gd<G, D>(smem);
 }
 
