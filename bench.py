@@ -48,7 +48,7 @@ DESCR = {
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=64)
+    p.add_argument("--steps", type=int, default=512)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["tkv", "reference"], default="tkv")
     p.add_argument("--workload", default="7b", choices=sorted(TARGET_N))
@@ -195,7 +195,9 @@ def cpu_baseline(args, steps=0):
 
 # -------------------------------------------------------------------- clocks
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 200 ms) with their timestamps; `stop(t0, t1)` keeps the
+    samples taken inside the wall-clock window [t0, t1] of the timed region."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -214,27 +216,34 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)          # let the sample after the window arrive
         self.proc.terminate()
         self.proc.wait()
         self.f.close()
-        rows = [l.split(",") for l in open(self.path) if l.strip()]
-        sm, mx, reasons = [], None, set()
+        import datetime
+        sm, mx, reasons, times = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
+        for line in open(self.path):
+            r = [x.strip() for x in line.split(",")]
             try:
-                sm.append(float(r[1]))
-                mx = float(r[2])
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(r[2]), float(r[3])
             except (ValueError, IndexError):
                 continue
-            for n, x in zip(names, r[5:9]):
+            times.append(ts)
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
+            sm.append(clk)
+            mx = cmax
+            for n, x in zip(names, r[6:10]):
                 if x.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window_s": (t1 - t0) if t0 is not None else None}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -347,12 +356,10 @@ def run_gpu(args, rank, world):
     def timed(c, r, t, sample_clocks):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
-        sampler = ClockSampler(dev) if (rank == 0 and sample_clocks) else None
-        if sampler:
-            sampler.start()
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
+        w0 = time.time()
         launches0 = c.stats()["kernel_launches"]
         captures0 = r.captures
         # marks the timed region for a profiler started with collection off (no-op otherwise)
@@ -365,14 +372,19 @@ def run_gpu(args, rank, world):
             r(t, *inputs[t - 1], graph)
             ev[i][1].record(stream)
         torch.cuda.synchronize()
+        w1 = time.time()
         if sample_clocks:
             torch.cuda.profiler.stop()
         if world > 1:
             torch.distributed.barrier()
-        clocks = sampler.stop() if sampler else None
+        clocks = sampler.stop(w0, w1) if (sampler and sample_clocks) else None
         step_ms = [x.elapsed_time(y) for x, y in ev]
         return (t, step_ms, clocks, c.stats()["kernel_launches"] - launches0, r.captures - captures0)
 
+    # clocks: sampled from before the lead-in; the samples inside the timed window are kept
+    sampler = ClockSampler(dev) if rank == 0 else None
+    if sampler:
+        sampler.start()
     ctx = new_context()
     run = Stepper(ctx)
     t, prof, prof_ms = lead_in(ctx, run, True)

@@ -89,6 +89,8 @@ struct tkv_ctx {
     int graph_steps_left = 0;
     int64_t graph_launches = 0, graph_t1_bytes = 0;
     int delta_max = 0;                 // pending delta moves (max over sequences), 0 = none
+    int delta_chunk = 1;               // layers per delta launch (about 1 MB of rows per launch)
+    int delta_next = 0;                // first layer whose delta is not enqueued yet
 
     int resident = 1;                  // attention CTAs resident on the device at once
     int last_splits = 0;
@@ -341,6 +343,16 @@ tkv_status run_retier(tkv_ctx* ctx, bool forced) {
     if (max_now > 0) ctx->launches++;
     CK(cudaEventRecord(ctx->ev_retier, ctx->compute));
     ctx->delta_max = max_delta;
+    // small deltas are gathered several layers per launch: each launch costs a host-link
+    // round trip and a launch, whatever it moves
+    {
+        int64_t rows = 0;
+        for (int b = 0; b < B; ++b) rows += ctx->h_outp[b].n_delta;
+        const int64_t per_layer = rows * (int64_t)row_bytes_bf16(ctx);
+        const int64_t want = int64_t(1) << 20;
+        ctx->delta_chunk = (int)std::min<int64_t>(ctx->L, std::max<int64_t>(1, per_layer > 0 ? (want + per_layer - 1) / per_layer : 1));
+        ctx->delta_next = 0;
+    }
 
     const int64_t rb = (int64_t)row_bytes_bf16(ctx) * ctx->L;
     ctx->st.last_promoted = k[MV_T1_T0] + k[MV_T2_T0];
@@ -422,9 +434,12 @@ tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
         }
     }
 t1_done:
-    if (ctx->delta_max > 0) {
-        tkv_status r = enqueue_delta(ctx, layer, layer + 1, ctx->copy);
+    if (ctx->delta_max > 0 && layer >= ctx->delta_next) {
+        // this layer's delta and the next ones' of its chunk, before this layer's T1 event
+        const int l1 = std::min(ctx->L, layer + ctx->delta_chunk);
+        tkv_status r = enqueue_delta(ctx, layer, l1, ctx->copy);
         if (r != TKV_OK) return r;
+        ctx->delta_next = l1;
     }
     CK(cudaEventRecord(ctx->ev_t1[slotr], ctx->copy));
     ctx->prefetched[layer] = 1;
