@@ -1,0 +1,103 @@
+"""Parity at full per-launch sizes, in the launch configuration the bench times
+(persistent grid, 256-row items, several items per CTA): the 14B-shaped stack
+(48 layers, batch 8, 40/8 heads, d 128, 4,096 positions) and the 70B-shaped
+layer (batch 8, 64/8 heads, 16,384 positions; 4 of its 80 layers).
+
+Every position is given a tier (T0 / T1 / T2 fp8 / T3 evicted, protected
+positions in T0), one decode step runs through the C ABI, and sampled
+(layer, sequence, KV head) groups are checked against the fp64 oracle computed
+for that group alone.  A second context with another T0/T1 split of the same
+positions (same T2 and T3 sets) must give bitwise the same outputs
+(Proposition 1)."""
+import numpy as np
+import pytest
+import torch
+
+import tiered_kv_cache_gqa_gb300 as tkv
+from oracle import attention, fp8, tiering
+from tiered_kv_cache_gqa_gb300 import synth
+
+from harness import ATOL_OUT, gpu_step
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # name: (workload, pre-filled positions (the decoded token adds one), layers, samples)
+    "14b": ("14b", 4095, None, [(0, 0, 0), (47, 7, 7), (23, 3, 5), (11, 5, 2), (36, 1, 4)]),
+    "70b": ("70b", 16383, 4, [(0, 0, 0), (3, 7, 7), (2, 4, 3)]),
+}
+
+
+def tier_map(WL, N, rng, t1_of_rest):
+    """T3 5 %, T2 15 %, then T1 takes `t1_of_rest` of what remains; protected positions stay T0."""
+    prot = tiering.protected_mask(N, WL.prompt_len, WL.num_sinks, WL.window)
+    free = np.nonzero(~prot)[0]
+    out = np.zeros((WL.batch, N), dtype=np.uint8)
+    for b in range(WL.batch):
+        p = rng.permutation(free)
+        n3, n2 = int(0.05 * len(p)), int(0.15 * len(p))
+        out[b, p[:n3]] = 3
+        out[b, p[n3:n3 + n2]] = 2
+        rest = p[n3 + n2:]
+        out[b, rest[: int(t1_of_rest * len(rest))]] = 1
+    return out
+
+
+def run(WL, N, gen, tiers, q, k, v):
+    ctx = tkv.TieredKV.for_workload(WL, t0_capacity=N + 8, t1_capacity=N, t2_capacity=N)
+    for l in range(WL.num_layers):
+        K, V = gen.prefill_layer(l)
+        ctx.append(l, K, V, N)
+        del K, V
+    ctx.set_tiers(tiers)
+    assert np.array_equal(ctx.tiers(), tiers)
+    out = torch.empty(WL.num_layers, WL.batch, WL.num_q_heads, WL.head_dim, device="cuda")
+    gpu_step(ctx, q, k, v, out)
+    res = out.cpu()
+    st = ctx.stats()
+    ctx.close()
+    return res, st
+
+
+def oracle_group(WL, N, gen, tiers, q, k, v, layer, b, kvh):
+    """fp64 attention of the group's G query heads over its retained rows."""
+    G, d = WL.group, WL.head_dim
+    kk, vv = gen.kv_rows(b, layer, 0, N)                       # [Hkv][N][d] bf16
+    K = torch.cat([kk[kvh], k[layer, b, kvh][None]]).float().cpu().numpy().astype(np.float64)
+    V = torch.cat([vv[kvh], v[layer, b, kvh][None]]).float().cpu().numpy().astype(np.float64)
+    t = np.append(tiers[b], 0)
+    for i in np.nonzero(t == 2)[0]:                             # T2: the row the kernel dequantises
+        for X in (K, V):
+            codes, scale = fp8.quantise_row(X[i].astype(np.float32))
+            X[i] = fp8.dequantise_row(codes, scale)
+    keep = t != 3
+    qh = q[layer, b, kvh * G:(kvh + 1) * G].float().cpu().numpy().astype(np.float64)
+    o, _ = attention.attend(qh, K[keep][:, None, :], V[keep][:, None, :], G)
+    return o
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_full_size_sampled_parity_and_proposition_1(case):
+    name, N, layers, samples = CASES[case]
+    WL = synth.WORKLOADS[name].with_(prefill_len=N, decode_steps=1, ratios=(0.3, 0.5, 0.15, 0.05), seed=77)
+    if layers:
+        WL = WL.with_(num_layers=layers)
+    gen = synth.Generator(WL, device="cuda")
+    q, k, v = gen.decode_step(1)
+    tiers_a = tier_map(WL, N, np.random.default_rng(1), 0.7)
+    out_a, st_a = run(WL, N, gen, tiers_a, q, k, v)
+    # the launch really is the bench's: several 256-row items per persistent CTA
+    assert st_a["attn_splits"] >= 152
+    for layer, b, kvh in samples:
+        ref = oracle_group(WL, N, gen, tiers_a, q, k, v, layer, b, kvh)
+        got = out_a[layer, b, kvh * WL.group:(kvh + 1) * WL.group].numpy()
+        err = np.abs(got - ref).max()
+        assert err <= ATOL_OUT, ((layer, b, kvh), err)
+    # Proposition 1: move T1 rows to T0 and T0 rows to T1, T2 and T3 untouched
+    tiers_b = tiers_a.copy()
+    prot = tiering.protected_mask(N, WL.prompt_len, WL.num_sinks, WL.window)
+    swap = (~prot)[None, :] & (tiers_a < 2)
+    tiers_b[swap] = 1 - tiers_a[swap]
+    out_b, st_b = run(WL, N, gen, tiers_b, q, k, v)
+    assert st_a["tier_count"][1] != st_b["tier_count"][1]
+    assert torch.equal(out_a, out_b)
