@@ -118,6 +118,7 @@ def synth_layers(name):
 
 
 # ------------------------------------------------------------------ oracle arm
+REF_MAX_SECONDS = 90.0   # the oracle arm stops sampling after this much CPU time
 def oracle_run(wl, n_steps, seconds):
     """Times the fp64 oracle's decode steps on this host (single-threaded BLAS).
 
@@ -141,7 +142,7 @@ def oracle_run(wl, n_steps, seconds):
             sess.step(*a)
             t_total += time.perf_counter() - t0
             done += 1
-            if not n_steps and t_total >= seconds:
+            if (not n_steps and t_total >= seconds) or t_total >= REF_MAX_SECONDS:
                 break
         return wl.batch * done / t_total, "%d full decode steps (all %d layers, batch %d)" % (
             done, wl.num_layers, wl.batch)
@@ -159,7 +160,7 @@ def oracle_run(wl, n_steps, seconds):
         t_total += time.perf_counter() - t0
         done += 1
         layer = (layer + 1) % wl.num_layers
-        if (n_steps and done >= n_steps) or (not n_steps and t_total >= seconds):
+        if (n_steps and done >= n_steps) or (not n_steps and t_total >= seconds) or t_total >= REF_MAX_SECONDS:
             break
     per_step = t_total / done * wl.num_layers * wl.batch
     return wl.batch / per_step, ("sampled: %d (sequence, layer) attention passes over %d positions, "
