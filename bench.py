@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--t3", type=float, default=None, help="eviction ratio")
     p.add_argument("--layers", type=int, default=None,
                    help="override the layer count (small captures for ncu; per-launch size unchanged)")
+    p.add_argument("--t2", choices=["hbm", "host"], default="hbm",
+                   help="where T2 (fp8) rows live: an HBM pool, or pinned host memory staged per layer")
     p.add_argument("--t1", choices=["ce", "sm", "split", "multi"], default="ce",
                    help="T1 transport: copy engine, SM copy kernel, or both")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -270,6 +272,7 @@ def run_gpu(args, rank, world):
     t1_mode = {"ce": tkv.TKV_T1_COPY_ENGINE, "sm": tkv.TKV_T1_SM_COPY, "split": tkv.TKV_T1_SPLIT,
                "multi": tkv.TKV_T1_MULTI_CE}[args.t1]
     graph = args.mode == "graph"
+    t2_place = tkv.TKV_T2_HOST if args.t2 == "host" else tkv.TKV_T2_HBM
     gen = synth.Generator(wl, device="cuda")
     n_steps = PRE_STEPS + args.warmup + args.steps + KP
     inputs = [gen.decode_step(t) for t in range(1, n_steps + 1)]
@@ -279,7 +282,7 @@ def run_gpu(args, rank, world):
     sq, sk, sv = (torch.empty_like(x) for x in inputs[0])
 
     def new_context():
-        c = tkv.TieredKV.for_workload(wl, device=dev, t1_transport=t1_mode)
+        c = tkv.TieredKV.for_workload(wl, device=dev, t1_transport=t1_mode, t2_placement=t2_place)
         for l in range(L):
             K, V = gen.prefill_layer(l)
             c.append(l, K, V, wl.prefill_len)
@@ -514,7 +517,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": describe(wl), "global_batch": wl.batch * world,
                    "seq_len": TARGET_N[args.workload], "parallelism": "replicas (sequence shards)",
-                   "t1_transport": args.t1, "steps_as": args.mode,
+                   "t1_transport": args.t1, "t2_placement": args.t2, "steps_as": args.mode,
                    "l2": "flushed between timed steps (256 MB write); step working set %.0f MB"
                          % (st["kv_bytes_full_cache"] / 2 ** 20)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
@@ -533,7 +536,9 @@ def main():
             "profiled_pass": {"steps": KP_, "mode": "eager", "ms_per_step": r["prof_ms"] / KP_,
                               "note": "per-kernel events; roofline and transfer figures come from this pass"},
             "attention_step_ms": pa["ms"] / KP_,
-            "t1_stream": {"gbs": t1_gbs, "bytes_per_step": p1["bytes"] / KP_, "ms_per_step": p1["ms"] / KP_},
+            "t1_stream": {"gbs": t1_gbs, "bytes_per_step": p1["bytes"] / KP_, "ms_per_step": p1["ms"] / KP_,
+                          "t2_bytes_total": st["h2d_bytes_t2_stream"],
+                          "note": "host-link stream per layer: T1 rows, and T2 records with --t2 host"},
             "delta_prefetch": {"gbs": delta_gbs, "bytes": pd["bytes"], "ms": pd["ms"]},
             "link_peak_gbs_nominal_pcie5x16": 64.0,
             "transfer_overhead_copy_share": link_ms / r["prof_ms"],

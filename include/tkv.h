@@ -73,6 +73,14 @@ typedef struct tkv_ctx tkv_ctx;
  *                       that several copy engines run at once */
 enum { TKV_T1_COPY_ENGINE = 0, TKV_T1_SM_COPY = 1, TKV_T1_SPLIT = 2, TKV_T1_MULTI_CE = 3 };
 
+/* Where the T2 rows (E4M3 codes + fp32 scales) live (tkv_config.t2_placement):
+ *   TKV_T2_HBM   in an HBM pool that the attention kernel reads in place
+ *   TKV_T2_HOST  in pinned host memory, the placement "Four-tier
+ *                classification" gives T2: each layer's T2 records are copied
+ *                with its T1 rows into an HBM staging ring before its attention.
+ * The same bytes reach the kernel either way, so the results are identical. */
+enum { TKV_T2_HBM = 0, TKV_T2_HOST = 1 };
+
 typedef struct {
     int32_t num_layers;       /* L >= 1 */
     int32_t num_q_heads;      /* Hq, a multiple of num_kv_heads, Hq / Hkv <= 8 */
@@ -98,6 +106,7 @@ typedef struct {
                                  non-blocking one (then order the caller's work with tkv_sync);
                                  cudaStreamLegacy / cudaStreamPerThread are accepted */
     void* copy_stream;        /* cudaStream_t for T1 prefetch and delta prefetch; NULL = create one */
+    int32_t t2_placement;     /* where T2 rows live: TKV_T2_HBM (0, default) or TKV_T2_HOST */
 } tkv_config;
 
 typedef struct {
@@ -121,6 +130,7 @@ typedef struct {
     int64_t kernel_launches;       /* kernels this context has launched (all kinds) */
     int32_t status;                /* tkv_status of the context */
     int32_t attn_splits;           /* CTAs of the last attention launch */
+    int64_t h2d_bytes_t2_stream;   /* cumulative bytes of the per-layer T2 stream (TKV_T2_HOST) */
 } tkv_stats;
 
 /* Creates a context: device pools for T0 (bf16), T2 (fp8 + scales) and the

@@ -49,14 +49,14 @@ def check_scores(s_gpu, s_ref):
         float(err.max()), float(bound[np.argmax(err - bound)]))
 
 
-def lockstep(wl, steps, device="cpu", check_out=True):
+def lockstep(wl, steps, device="cpu", check_out=True, **ctx_kw):
     """Runs `steps` decode steps on both sides; re-tier every wl.delta steps.
 
     The re-tier is checked bit-exactly by feeding the GPU's fp32 scores to the
     oracle's tier assignment; both sides then continue from the same tiers.
     Returns (ctx, sess, worst output error)."""
     gen = synth.Generator(wl, device=device)
-    ctx = tkv.TieredKV.for_workload(wl)
+    ctx = tkv.TieredKV.for_workload(wl, **ctx_kw)
     sess = make_session(wl)
     prefill_both(ctx, sess, gen)
     L, B, Hq, d = wl.num_layers, wl.batch, wl.num_q_heads, wl.head_dim

@@ -59,3 +59,22 @@ def test_create_rejects_bad_config_without_touching_a_gpu(lib_path):
     cfg.head_dim, cfg.ratio_t0 = 64, 0.5                                                # ratios sum
     assert lib.tkv_create(ctypes.byref(cfg), ctypes.byref(ctx)) == tkv.TKV_EINVAL
     assert lib.tkv_append(None, 0, None, None, 1) == tkv.TKV_EINVAL
+
+
+def header_struct_fields(name):
+    """Field names, in order, of `typedef struct { ... } name;` in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\}\s*" + name + r"\s*;", text).group(1)
+    names = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if decl:
+            names.append(re.match(r".*?\b(\w+)\s*(\[\w+\])?$", decl, flags=re.S).group(1))
+    return names
+
+
+@pytest.mark.parametrize("cname,pyname", [("tkv_config", "Config"), ("tkv_stats", "Stats"),
+                                          ("tkv_prof_entry", "ProfEntry")])
+def test_binding_structs_match_the_header(cname, pyname):
+    import tiered_kv_cache_gqa_gb300 as tkv
+    assert [f[0] for f in getattr(tkv, pyname)._fields_] == header_struct_fields(cname)

@@ -255,3 +255,39 @@ def test_t1_transports_are_bitwise_identical():
     for o, s, _ in outs[1:]:
         assert torch.equal(o, outs[0][0])
         assert np.array_equal(s, outs[0][1])
+
+
+def test_t2_on_host_matches_t2_in_hbm_bitwise_and_the_oracle():
+    """T2 records in pinned host memory, staged per layer with the T1 rows, against the HBM
+    pool: the kernel reads the same bytes, so outputs, scores, tiers and stored records are
+    identical; the host placement also runs in lockstep with the oracle."""
+    wl = synth.Workload("t2host", 3, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
+                        window=16, ratios=(0.3, 0.4, 0.25, 0.05), outlier_rate=0.01, seed=9)
+    runs = []
+    for place in (tkv.TKV_T2_HBM, tkv.TKV_T2_HOST):
+        gen = synth.Generator(wl)
+        ctx = tkv.TieredKV.for_workload(wl, t2_placement=place)
+        prefill_both(ctx, None, gen)
+        out = torch.empty(wl.num_layers, wl.batch, wl.num_q_heads, wl.head_dim, device="cuda")
+        res = []
+        for t in range(1, 71):
+            q, k, v = gen.decode_step(t)
+            gpu_step(ctx, q.cuda(), k.cuda(), v.cuda(), out)
+            if t % 64 == 0:
+                ctx.retier()
+            if t > 64:
+                res.append(out.cpu().clone())
+        tiers = ctx.tiers()
+        recs = [ctx.row(l, b, int(i)) for l in range(wl.num_layers) for b in range(wl.batch)
+                for i in np.nonzero(tiers[b] == 2)[0][:20]]
+        runs.append((torch.stack(res), ctx.scores(), tiers, ctx.stats(), recs))
+    (o0, s0, t0, st0, r0), (o1, s1, t1, st1, r1) = runs
+    assert (t0 == 2).sum() > 100
+    assert torch.equal(o0, o1)
+    assert np.array_equal(s0, s1) and np.array_equal(t0, t1)
+    assert st0["h2d_bytes_t2_stream"] == 0 < st1["h2d_bytes_t2_stream"]
+    assert st1["hbm_bytes_kv_resident"] < st0["hbm_bytes_kv_resident"]
+    for (ta, ca, sa), (tb, cb, sb) in zip(r0, r1):
+        assert ta == tb == 2 and np.array_equal(ca, cb) and np.array_equal(sa, sb)
+    _, _, worst = lockstep(wl, 70, t2_placement=tkv.TKV_T2_HOST)
+    assert worst <= ATOL_OUT

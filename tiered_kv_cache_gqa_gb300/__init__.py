@@ -20,6 +20,7 @@ LIB_PATH = os.environ.get("TKV_LIBRARY") or os.path.join(_HERE, "libtkv.so")
 
 TKV_OK, TKV_EINVAL, TKV_ENOMEM, TKV_ECUDA, TKV_ECAPACITY, TKV_ETIMEOUT, TKV_ESTATE = range(7)
 TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY, TKV_T1_SPLIT, TKV_T1_MULTI_CE = range(4)
+TKV_T2_HBM, TKV_T2_HOST = range(2)
 
 # Every function the C ABI exports (include/tkv.h).
 EXPORTS = ("tkv_create", "tkv_destroy", "tkv_append", "tkv_prefetch", "tkv_decode_step",
@@ -52,6 +53,7 @@ class Config(ctypes.Structure):
         ("t2_capacity", ctypes.c_int32), ("t1_transport", ctypes.c_int32),
         ("device", ctypes.c_int32),
         ("compute_stream", ctypes.c_void_p), ("copy_stream", ctypes.c_void_p),
+        ("t2_placement", ctypes.c_int32),
     ]
 
 
@@ -67,6 +69,7 @@ class Stats(ctypes.Structure):
         ("hbm_bytes_kv_resident", ctypes.c_int64), ("kv_bytes_full_cache", ctypes.c_int64),
         ("kernel_launches", ctypes.c_int64),
         ("status", ctypes.c_int32), ("attn_splits", ctypes.c_int32),
+        ("h2d_bytes_t2_stream", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -263,7 +266,8 @@ class TieredKV:
     def __init__(self, *, num_layers, num_q_heads, num_kv_heads, head_dim, batch, max_tokens,
                  prompt_len, num_sinks=4, recent_window=64, retier_interval=64,
                  ratios=(1.0, 0.0, 0.0, 0.0), t0_capacity=0, t1_capacity=0, t2_capacity=0,
-                 t1_transport=TKV_T1_COPY_ENGINE, device=0, compute_stream=None, copy_stream=None):
+                 t1_transport=TKV_T1_COPY_ENGINE, device=0, compute_stream=None, copy_stream=None,
+                 t2_placement=TKV_T2_HBM):
         cfg = Config()
         cfg.num_layers, cfg.num_q_heads, cfg.num_kv_heads = num_layers, num_q_heads, num_kv_heads
         cfg.head_dim, cfg.batch, cfg.max_tokens = head_dim, batch, max_tokens
@@ -272,6 +276,7 @@ class TieredKV:
         cfg.ratio_t0, cfg.ratio_t1, cfg.ratio_t2, cfg.ratio_t3 = ratios
         cfg.t0_capacity, cfg.t1_capacity, cfg.t2_capacity = t0_capacity, t1_capacity, t2_capacity
         cfg.t1_transport = t1_transport
+        cfg.t2_placement = t2_placement
         cfg.device = device
         if compute_stream is None:
             compute_stream = torch_stream_handle()

@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                     row_v = stg + row_index(0, 1, b, kvh, slot, a.B, a.Hkv, a.S1) * (2 * D);
                     row_bytes = 2 * D;
                 } else {
-                    src = a.t2 + row_index(a.layer, 0, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
-                    row_v = a.t2 + row_index(a.layer, 1, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
+                    src = a.t2 + row_index(a.t2_layer, 0, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
+                    row_v = a.t2 + row_index(a.t2_layer, 1, b, kvh, slot, a.B, a.Hkv, a.S2) * (D + 16);
                     row_bytes = D + 16;
                     fp8 = true;
                 }

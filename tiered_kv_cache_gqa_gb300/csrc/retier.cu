@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kRetierThreads) retier_kernel(const RetierArgs
     __syncthreads();
 
     // ---- phase C/D: retained list, move lists, counters
-    int hw = 0, r = 0, mn = 0, md = 0;
+    int hw = 0, hw2 = 0, r = 0, mn = 0, md = 0;
     int kind_cnt[7] = {0, 0, 0, 0, 0, 0, 0};
     int cnt_t[4] = {0, 0, 0, 0};
     auto kind_of = [](int o, int n) {
@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(kRetierThreads) retier_kernel(const RetierArgs
         if (n == 3) continue;
         ++r;
         if (n == 1) hw = max(hw, new_s[i] + 1);
+        if (n == 2) hw2 = max(hw2, new_s[i] + 1);
         const int kd = kind_of(o, n);
         if (kd) {
             kind_cnt[kd]++;
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(kRetierThreads) retier_kernel(const RetierArgs
         }
     }
     const int HW = block_max(hw, tmp);
+    const int HW2 = block_max(hw2, tmp);
     for (int t = 0; t < 4; ++t) atomicAdd(&tier_count[t], cnt_t[t]);
     for (int kd = 0; kd < 7; ++kd) {
         int tot;
@@ -292,6 +294,7 @@ __global__ void __launch_bounds__(kRetierThreads) retier_kernel(const RetierArgs
         a.outp[b].n_now = MN;
         a.outp[b].n_delta = MD;
         a.outp[b].hw1 = HW;
+        a.outp[b].hw2 = HW2;
         for (int t = 0; t < 4; ++t) a.outp[b].count[t] = tier_count[t];
         a.outp[b].error = err;
     }

@@ -35,7 +35,9 @@ struct tkv_ctx {
     // device
     __nv_bfloat16* k0v0 = nullptr;
     __nv_bfloat16* stage = nullptr;
-    uint8_t* t2 = nullptr;
+    uint8_t* t2 = nullptr;                   // T2 pool (HBM), or the device view of the host pool
+    uint8_t* t2_host = nullptr;              // TKV_T2_HOST: the pinned host pool
+    uint8_t* stage2 = nullptr;               // TKV_T2_HOST: T2 staging ring [2][2][B][Hkv][S2][d+16]
     uint8_t *tier = nullptr, *new_tier = nullptr, *forced = nullptr;
     int32_t *slot = nullptr, *new_slot = nullptr, *free_scratch = nullptr;
     float* s = nullptr;
@@ -64,6 +66,7 @@ struct tkv_ctx {
     std::vector<int> count[4];         // tokens per tier, per sequence
     std::vector<int> R;                // retained positions, per sequence
     int hw1 = 0;                       // T1 slots streamed per layer
+    int hw2 = 0;                       // T2 slots streamed per layer (TKV_T2_HOST)
     int64_t step = 0, retiers = 0;
 
     // protocol state
@@ -87,7 +90,7 @@ struct tkv_ctx {
     } cap_saved;
     cudaGraphExec_t graph_exec = nullptr;
     int graph_steps_left = 0;
-    int64_t graph_launches = 0, graph_t1_bytes = 0;
+    int64_t graph_launches = 0, graph_t1_bytes = 0, graph_t2_bytes = 0;
     int delta_max = 0;                 // pending delta moves (max over sequences), 0 = none
     int delta_chunk = 1;               // layers per delta launch (about 1 MB of rows per launch)
     int delta_next = 0;                // first layer whose delta is not enqueued yet
@@ -175,7 +178,9 @@ int protected_count(int N, int prompt, int sinks, int W) {
 size_t row_bytes_bf16(const tkv_ctx* c) { return (size_t)2 * c->Hkv * c->d * 2; }   // K+V, one layer
 
 void free_all(tkv_ctx* c) {
-    cudaFree(c->k0v0); cudaFree(c->stage); cudaFree(c->t2);
+    cudaFree(c->k0v0); cudaFree(c->stage); cudaFree(c->stage2);
+    if (c->t2_host) cudaFreeHost(c->t2_host);
+    else cudaFree(c->t2);
     cudaFree(c->tier); cudaFree(c->new_tier); cudaFree(c->forced);
     cudaFree(c->slot); cudaFree(c->new_slot); cudaFree(c->free_scratch);
     cudaFree(c->s); cudaFree(c->rl_loc); cudaFree(c->rl_pos); cudaFree(c->rl_count);
@@ -316,7 +321,7 @@ tkv_status run_retier(tkv_ctx* ctx, bool forced) {
     tkv_status ds = read_device_status(ctx);
     if (ds != TKV_OK) return ds;
 
-    int hw = 0, max_now = 0, max_delta = 0;
+    int hw = 0, hw2 = 0, max_now = 0, max_delta = 0;
     int64_t k[8] = {0};
     for (int b = 0; b < B; ++b) {
         const RetierOut& o = ctx->h_outp[b];
@@ -324,11 +329,13 @@ tkv_status run_retier(tkv_ctx* ctx, bool forced) {
         for (int t = 0; t < 4; ++t) ctx->count[t][b] = o.count[t];
         ctx->R[b] = N - o.count[3];
         hw = std::max(hw, o.hw1);
+        hw2 = std::max(hw2, o.hw2);
         max_now = std::max(max_now, o.n_now);
         max_delta = std::max(max_delta, o.n_delta);
         for (int q = 0; q < 7; ++q) k[q] += o.kinds[q];
     }
     ctx->hw1 = hw;
+    ctx->hw2 = hw2;
     // rows leaving T0 / entering T2 or T1 from the host side: now, all layers
     MoveArgs m{};
     m.moves = ctx->moves_now;
@@ -434,6 +441,20 @@ tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
         }
     }
 t1_done:
+    if (ctx->t2_host && ctx->hw2 > 0) {
+        // T2 records of the layer, rows [0, hw2) of every (K/V, sequence, head), into staging slot layer % 2
+        const size_t rec = (size_t)ctx->d + 16;
+        const size_t pitch = (size_t)ctx->S2 * rec;
+        const size_t layer_bytes = (size_t)2 * ctx->B * ctx->Hkv * pitch;
+        const size_t width = (size_t)ctx->hw2 * rec;
+        const int height = 2 * ctx->B * ctx->Hkv;
+        const bool timed = prof_open(ctx, 1, ctx->copy);
+        CK(cudaMemcpy2DAsync(ctx->stage2 + (size_t)slotr * layer_bytes, pitch,
+                             ctx->t2_host + (size_t)layer * layer_bytes, pitch, width, height,
+                             cudaMemcpyHostToDevice, ctx->copy));
+        if (timed) prof_close(ctx, 1, ctx->copy, (double)(width * height));
+        ctx->st.h2d_bytes_t2_stream += (int64_t)(width * height);
+    }
     if (ctx->delta_max > 0 && layer >= ctx->delta_next) {
         // this layer's delta and the next ones' of its chunk, before this layer's T1 event
         const int l1 = std::min(ctx->L, layer + ctx->delta_chunk);
@@ -475,6 +496,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     if (c.prompt_len < 0 || c.num_sinks < 0 || c.recent_window < 0) return TKV_EINVAL;
     if (c.t0_capacity < 0 || c.t1_capacity < 0 || c.t2_capacity < 0) return TKV_EINVAL;
     if (c.t1_transport < TKV_T1_COPY_ENGINE || c.t1_transport > TKV_T1_MULTI_CE) return TKV_EINVAL;
+    if (c.t2_placement != TKV_T2_HBM && c.t2_placement != TKV_T2_HOST) return TKV_EINVAL;
     const float r[4] = {c.ratio_t0, c.ratio_t1, c.ratio_t2, c.ratio_t3};
     int64_t ppm[4], sum = 0;
     for (int i = 0; i < 4; ++i) {
@@ -527,7 +549,9 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     };
     A(dalloc(ctx, &ctx->k0v0, L * 2 * B * Hkv * S0 * d));
     A(dalloc(ctx, &ctx->stage, 2 * 2 * B * Hkv * S1 * d));
-    A(dalloc(ctx, &ctx->t2, L * 2 * B * Hkv * S2 * (d + 16)));
+    const bool t2_host = c.t2_placement == TKV_T2_HOST;
+    if (!t2_host) A(dalloc(ctx, &ctx->t2, L * 2 * B * Hkv * S2 * (d + 16)));
+    else A(dalloc(ctx, &ctx->stage2, 2 * 2 * B * Hkv * S2 * (d + 16)));
     A(dalloc(ctx, &ctx->tier, B * Nmax));
     A(dalloc(ctx, &ctx->new_tier, B * Nmax));
     A(dalloc(ctx, &ctx->forced, B * Nmax));
@@ -554,6 +578,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     }
     A(halloc(ctx, &ctx->h1, L * 2 * B * Hkv * S1 * d));
     A(halloc(ctx, &ctx->h2m, L * 2 * B * Hkv * S2 * d));
+    if (t2_host) A(halloc(ctx, &ctx->t2_host, L * 2 * B * Hkv * S2 * (d + 16)));
     A(halloc(ctx, &ctx->h_outp, B));
     A(halloc(ctx, &ctx->h_params, B));
     A(halloc(ctx, &ctx->h_err, 1));
@@ -563,6 +588,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     }
     if (ctx->h1 && cudaHostGetDevicePointer((void**)&ctx->d_h1, ctx->h1, 0) != cudaSuccess) return bail(TKV_ECUDA);
     if (ctx->h2m && cudaHostGetDevicePointer((void**)&ctx->d_h2m, ctx->h2m, 0) != cudaSuccess) return bail(TKV_ECUDA);
+    if (ctx->t2_host && cudaHostGetDevicePointer((void**)&ctx->t2, ctx->t2_host, 0) != cudaSuccess) return bail(TKV_ECUDA);
     std::memset(ctx->h_outp, 0, B * sizeof(RetierOut));
 
     // page tables: empty; T0 free stack holds every slot, lowest on top
@@ -714,7 +740,13 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
     a.out = out;
     a.k0v0 = ctx->k0v0;
     a.stage = ctx->stage + (size_t)slotr * 2 * ctx->B * ctx->Hkv * ctx->S1 * ctx->d;
-    a.t2 = ctx->t2;
+    if (ctx->t2_host) {
+        a.t2 = ctx->stage2 + (size_t)slotr * 2 * ctx->B * ctx->Hkv * ctx->S2 * (ctx->d + 16);
+        a.t2_layer = 0;
+    } else {
+        a.t2 = ctx->t2;
+        a.t2_layer = layer;
+    }
     a.new_k = (const __nv_bfloat16*)ctx->pend_k[layer];
     a.new_v = (const __nv_bfloat16*)ctx->pend_v[layer];
     ctx->pend_k[layer] = ctx->pend_v[layer] = nullptr;
@@ -855,9 +887,14 @@ tkv_status tkv_get_row(tkv_ctx* ctx, int32_t layer, int32_t seq, int32_t pos, vo
                             ctx->h1 + row_index(layer, kv, seq, h, sl, ctx->B, ctx->Hkv, ctx->S1) * d,
                             (size_t)d * 2);
             } else if (t == 2) {
-                const uint8_t* rec = ctx->t2 + row_index(layer, kv, seq, h, sl, ctx->B, ctx->Hkv, ctx->S2) * (d + 16);
-                CK(cudaMemcpy((uint8_t*)dst + o * d, rec, (size_t)d, cudaMemcpyDeviceToHost));
-                if (scales) CK(cudaMemcpy(scales + o, rec + d, 4, cudaMemcpyDeviceToHost));
+                const size_t ri = row_index(layer, kv, seq, h, sl, ctx->B, ctx->Hkv, ctx->S2) * (d + 16);
+                if (ctx->t2_host) {
+                    std::memcpy((uint8_t*)dst + o * d, ctx->t2_host + ri, (size_t)d);
+                    if (scales) std::memcpy(scales + o, ctx->t2_host + ri + d, 4);
+                } else {
+                    CK(cudaMemcpy((uint8_t*)dst + o * d, ctx->t2 + ri, (size_t)d, cudaMemcpyDeviceToHost));
+                    if (scales) CK(cudaMemcpy(scales + o, ctx->t2 + ri + d, 4, cudaMemcpyDeviceToHost));
+                }
             }
         }
     }
@@ -943,6 +980,7 @@ tkv_status tkv_capture_end(tkv_ctx* ctx, int32_t* steps_valid) {
     const bool one_step = ctx->open_n == 0 && ctx->step == ctx->cap_saved.step + 1;
     const int64_t launches = ctx->launches - ctx->cap_saved.launches;
     const int64_t t1 = ctx->st.h2d_bytes_t1_stream - ctx->cap_saved.st.h2d_bytes_t1_stream;
+    const int64_t t2b = ctx->st.h2d_bytes_t2_stream - ctx->cap_saved.st.h2d_bytes_t2_stream;
     // nothing of the captured step has run: back to the state before it
     ctx->N = ctx->cap_saved.N;
     ctx->count[0] = ctx->cap_saved.count0;
@@ -985,6 +1023,7 @@ tkv_status tkv_capture_end(tkv_ctx* ctx, int32_t* steps_valid) {
     ctx->graph_steps_left = valid;
     ctx->graph_launches = launches;
     ctx->graph_t1_bytes = t1;
+    ctx->graph_t2_bytes = t2b;
     if (steps_valid) *steps_valid = valid;
     return TKV_OK;
 }
@@ -1005,6 +1044,7 @@ tkv_status tkv_replay(tkv_ctx* ctx) {
     ctx->step++;
     ctx->launches += ctx->graph_launches;
     ctx->st.h2d_bytes_t1_stream += ctx->graph_t1_bytes;
+    ctx->st.h2d_bytes_t2_stream += ctx->graph_t2_bytes;
     ctx->graph_steps_left--;
     return TKV_OK;
 }
@@ -1033,7 +1073,10 @@ tkv_status tkv_get_stats(tkv_ctx* ctx, tkv_stats* out) {
     s.host_bytes_allocated = (int64_t)ctx->host_alloc;
     const int64_t rb = (int64_t)row_bytes_bf16(ctx) * ctx->L;
     const int64_t r2 = (int64_t)2 * ctx->Hkv * (ctx->d + 16) * ctx->L;
-    s.hbm_bytes_kv_resident = s.tier_count[0] * rb + s.tier_count[2] * r2 +
+    // T0 rows, T2 records in HBM (or their two staged layers), and the two staged layers of T1
+    const int64_t t2_in_hbm = ctx->t2_host ? (int64_t)2 * ctx->B * ctx->hw2 * 2 * ctx->Hkv * (ctx->d + 16)
+                                           : s.tier_count[2] * r2;
+    s.hbm_bytes_kv_resident = s.tier_count[0] * rb + t2_in_hbm +
                               (int64_t)2 * ctx->B * ctx->hw1 * (int64_t)row_bytes_bf16(ctx);
     s.kv_bytes_full_cache = (int64_t)ctx->N * ctx->B * rb;
     s.kernel_launches = ctx->launches;

@@ -39,6 +39,7 @@ struct RetierOut {
     int32_t n_now;        // moves applied at re-tier time
     int32_t n_delta;      // moves left for the delta prefetch
     int32_t hw1;          // highest referenced T1 slot + 1
+    int32_t hw2;          // highest referenced T2 slot + 1
     int32_t count[4];     // tokens per tier after the re-tier
     int32_t kinds[8];     // moves per kind
     int32_t error;        // 0 or a tkv_status
@@ -156,7 +157,8 @@ struct AttnArgs {
     float* out;                  // [B][Hq][d]
     const __nv_bfloat16* k0v0;   // T0 pool (all layers)
     const __nv_bfloat16* stage;  // staging ring slot for this layer: [2][B][Hkv][S1][d]
-    const uint8_t* t2;           // T2 pool (all layers)
+    const uint8_t* t2;           // T2 records: the pool (all layers) or this layer's staging slot
+    int t2_layer;                // layer index into t2: `layer` for the pool, 0 for a staging slot
     const __nv_bfloat16* new_k;  // [B][Hkv][d] this layer's decode-token K, written to its T0 slot
     const __nv_bfloat16* new_v;  //   by the CTA that owns the row (null: nothing to write)
     const uint32_t* rl_loc;      // [B][Nmax]
