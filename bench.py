@@ -58,8 +58,9 @@ def parse():
                    help="override the layer count (small captures for ncu; per-launch size unchanged)")
     p.add_argument("--t2", choices=["hbm", "host"], default="hbm",
                    help="where T2 (fp8) rows live: an HBM pool, or pinned host memory staged per layer")
-    p.add_argument("--t1", choices=["ce", "sm", "split", "multi"], default="ce",
-                   help="T1 transport: copy engine, SM copy kernel, or both")
+    p.add_argument("--t1", choices=["ce", "sm", "split", "multi", "resident"], default="ce",
+                   help="T1 transport: copy engine, SM copy kernel, both, four copy streams, or an "
+                        "HBM-resident copy updated by the re-tier (only the delta crosses the link)")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -270,7 +271,7 @@ def run_gpu(args, rank, world):
     L, B, Hq, Hkv, d = wl.num_layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     stream = torch.cuda.current_stream()
     t1_mode = {"ce": tkv.TKV_T1_COPY_ENGINE, "sm": tkv.TKV_T1_SM_COPY, "split": tkv.TKV_T1_SPLIT,
-               "multi": tkv.TKV_T1_MULTI_CE}[args.t1]
+               "multi": tkv.TKV_T1_MULTI_CE, "resident": tkv.TKV_T1_RESIDENT}[args.t1]
     graph = args.mode == "graph"
     t2_place = tkv.TKV_T2_HOST if args.t2 == "host" else tkv.TKV_T2_HBM
     gen = synth.Generator(wl, device="cuda")

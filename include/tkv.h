@@ -70,8 +70,14 @@ typedef struct tkv_ctx tkv_ctx;
  *   TKV_T1_SPLIT        half the rows by the copy engine, half by the copy
  *                       kernel on a second stream, concurrently
  *   TKV_T1_MULTI_CE     the rows split four ways over four copy streams, so
- *                       that several copy engines run at once */
-enum { TKV_T1_COPY_ENGINE = 0, TKV_T1_SM_COPY = 1, TKV_T1_SPLIT = 2, TKV_T1_MULTI_CE = 3 };
+ *                       that several copy engines run at once
+ *   TKV_T1_RESIDENT     the other reading of "System implementation": an HBM
+ *                       copy of every layer's T1 rows is kept next to the host
+ *                       store and updated by the re-tier's moves, so only the
+ *                       delta crosses the host link (no per-step T1 stream;
+ *                       T1 then occupies HBM like T0) */
+enum { TKV_T1_COPY_ENGINE = 0, TKV_T1_SM_COPY = 1, TKV_T1_SPLIT = 2, TKV_T1_MULTI_CE = 3,
+       TKV_T1_RESIDENT = 4 };
 
 /* Where the T2 rows (E4M3 codes + fp32 scales) live (tkv_config.t2_placement):
  *   TKV_T2_HBM   in an HBM pool that the attention kernel reads in place
@@ -288,7 +294,7 @@ tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, float* out, f
  * between launches) off a decode step.
  * tkv_capture_begin: between decode steps, with no delta prefetch pending
  * (i.e. not on the first step after a re-tier), profiling off and the T1
- * transport TKV_T1_COPY_ENGINE or TKV_T1_SM_COPY.  The caller then makes one
+ * transport TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY or TKV_T1_RESIDENT.  The caller then makes one
  * decode step's calls (tkv_append / tkv_prefetch / tkv_decode_step for every
  * layer) as usual: they are recorded into a graph, on an internal stream, and
  * nothing runs.  tkv_capture_end instantiates the graph, puts the context back

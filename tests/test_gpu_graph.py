@@ -59,7 +59,7 @@ def run(use_graph, t1_mode):
     return res, replays, captures, ctx
 
 
-@pytest.mark.parametrize("t1_mode", [tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T1_SM_COPY])
+@pytest.mark.parametrize("t1_mode", [tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T1_SM_COPY, tkv.TKV_T1_RESIDENT])
 def test_replayed_steps_match_eager_steps_bitwise(t1_mode):
     ref, _, _, _ = run(False, tkv.TKV_T1_COPY_ENGINE)
     got, replays, captures, ctx = run(True, t1_mode)

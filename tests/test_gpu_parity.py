@@ -232,12 +232,14 @@ def test_call_order_and_capacity_errors_leave_context_usable():
 
 
 def test_t1_transports_are_bitwise_identical():
-    """Copy engine, SM copy kernel and the split of both put the same bytes in the same staging
-    rows: outputs and scores are bit-identical, and match the oracle."""
+    """Copy engine, SM copy kernel, the split of both, four copy streams and the HBM-resident
+    copy kept by the re-tier put the same bytes in the rows the kernel reads: outputs and scores
+    are bit-identical, and match the oracle.  The resident copy streams nothing per step."""
     wl = synth.Workload("t1x", 3, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
                         window=16, ratios=(0.3, 0.6, 0.05, 0.05), seed=8)
     outs = []
-    for mode in (tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T1_SM_COPY, tkv.TKV_T1_SPLIT, tkv.TKV_T1_MULTI_CE):
+    for mode in (tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T1_SM_COPY, tkv.TKV_T1_SPLIT, tkv.TKV_T1_MULTI_CE,
+                 tkv.TKV_T1_RESIDENT):
         gen = synth.Generator(wl)
         ctx = tkv.TieredKV.for_workload(wl, t1_transport=mode)
         prefill_both(ctx, None, gen)
@@ -251,7 +253,7 @@ def test_t1_transports_are_bitwise_identical():
             if t > 64:
                 res.append(out.cpu().clone())
         outs.append((torch.stack(res), ctx.scores(), ctx.stats()["h2d_bytes_t1_stream"]))
-    assert outs[0][2] > 0
+    assert outs[0][2] > 0 and outs[-1][2] == 0
     for o, s, _ in outs[1:]:
         assert torch.equal(o, outs[0][0])
         assert np.array_equal(s, outs[0][1])

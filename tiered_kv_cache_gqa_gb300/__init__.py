@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("TKV_LIBRARY") or os.path.join(_HERE, "libtkv.so")
 
 TKV_OK, TKV_EINVAL, TKV_ENOMEM, TKV_ECUDA, TKV_ECAPACITY, TKV_ETIMEOUT, TKV_ESTATE = range(7)
-TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY, TKV_T1_SPLIT, TKV_T1_MULTI_CE = range(4)
+TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY, TKV_T1_SPLIT, TKV_T1_MULTI_CE, TKV_T1_RESIDENT = range(5)
 TKV_T2_HBM, TKV_T2_HOST = range(2)
 
 # Every function the C ABI exports (include/tkv.h).

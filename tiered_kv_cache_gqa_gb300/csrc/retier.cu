@@ -352,9 +352,11 @@ __global__ void __launch_bounds__(128) moves_kernel(const MoveArgs a) {
             const bool live = row < 2 * a.Hkv;   // uniform within a row group
             const int kv = live ? row / a.Hkv : 0, h = live ? row % a.Hkv : 0;
             if (kind == MV_T0_T1 || kind == MV_T2_T1) {
-                if (live)
-                    *reinterpret_cast<uint4*>(a.h1 + row_index(layer, kv, b, h, dst, a.B, a.Hkv, a.S1) * D +
-                                              sub * 8) = w[it];
+                if (live) {
+                    const size_t ri = row_index(layer, kv, b, h, dst, a.B, a.Hkv, a.S1) * D + sub * 8;
+                    *reinterpret_cast<uint4*>(a.h1 + ri) = w[it];
+                    if (a.t1_res) *reinterpret_cast<uint4*>(a.t1_res + ri) = w[it];   // the resident copy too
+                }
             } else if (kind == MV_T1_T0 || kind == MV_T2_T0) {
                 if (live)
                     *reinterpret_cast<uint4*>(a.k0v0 + row_index(layer, kv, b, h, dst, a.B, a.Hkv, a.S0) * D +

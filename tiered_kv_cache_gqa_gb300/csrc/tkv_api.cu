@@ -258,6 +258,7 @@ tkv_status enqueue_delta(tkv_ctx* ctx, int l0, int l1, cudaStream_t st) {
     m.counts = &ctx->outp[0].n_delta;
     m.count_stride = (int)(sizeof(RetierOut) / sizeof(int32_t));
     m.k0v0 = ctx->k0v0; m.t2 = ctx->t2; m.h1 = ctx->d_h1; m.h2m = ctx->d_h2m;
+    m.t1_res = ctx->cfg.t1_transport == TKV_T1_RESIDENT ? ctx->stage : nullptr;
     m.layer_begin = l0; m.layer_end = l1;
     m.L = ctx->L; m.B = ctx->B; m.Hkv = ctx->Hkv; m.d = ctx->d; m.Nmax = ctx->Nmax;
     m.S0 = ctx->S0; m.S1 = ctx->S1; m.S2 = ctx->S2;
@@ -342,6 +343,7 @@ tkv_status run_retier(tkv_ctx* ctx, bool forced) {
     m.counts = &ctx->outp[0].n_now;
     m.count_stride = (int)(sizeof(RetierOut) / sizeof(int32_t));
     m.k0v0 = ctx->k0v0; m.t2 = ctx->t2; m.h1 = ctx->d_h1; m.h2m = ctx->d_h2m;
+    m.t1_res = ctx->cfg.t1_transport == TKV_T1_RESIDENT ? ctx->stage : nullptr;
     m.layer_begin = 0; m.layer_end = ctx->L;
     m.L = ctx->L; m.B = B; m.Hkv = ctx->Hkv; m.d = ctx->d; m.Nmax = ctx->Nmax;
     m.S0 = ctx->S0; m.S1 = ctx->S1; m.S2 = ctx->S2;
@@ -386,7 +388,7 @@ tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
         CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_attn[slotr], 0));
         CK(cudaStreamWaitEvent(ctx->copy, ctx->ev_retier, 0));
     }
-    if (ctx->hw1 > 0) {
+    if (ctx->hw1 > 0 && ctx->cfg.t1_transport != TKV_T1_RESIDENT) {
         const size_t pitch = (size_t)ctx->S1 * ctx->d * sizeof(__nv_bfloat16);
         const size_t layer_elems = (size_t)2 * ctx->B * ctx->Hkv * ctx->S1 * ctx->d;
         const __nv_bfloat16* src = ctx->h1 + (size_t)layer * layer_elems;
@@ -495,7 +497,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     if (c.max_tokens < 1 || c.max_tokens > 65536) return TKV_EINVAL;
     if (c.prompt_len < 0 || c.num_sinks < 0 || c.recent_window < 0) return TKV_EINVAL;
     if (c.t0_capacity < 0 || c.t1_capacity < 0 || c.t2_capacity < 0) return TKV_EINVAL;
-    if (c.t1_transport < TKV_T1_COPY_ENGINE || c.t1_transport > TKV_T1_MULTI_CE) return TKV_EINVAL;
+    if (c.t1_transport < TKV_T1_COPY_ENGINE || c.t1_transport > TKV_T1_RESIDENT) return TKV_EINVAL;
     if (c.t2_placement != TKV_T2_HBM && c.t2_placement != TKV_T2_HOST) return TKV_EINVAL;
     const float r[4] = {c.ratio_t0, c.ratio_t1, c.ratio_t2, c.ratio_t3};
     int64_t ppm[4], sum = 0;
@@ -548,7 +550,8 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
         if (e != cudaSuccess) ok = false;
     };
     A(dalloc(ctx, &ctx->k0v0, L * 2 * B * Hkv * S0 * d));
-    A(dalloc(ctx, &ctx->stage, 2 * 2 * B * Hkv * S1 * d));
+    // T1 staging: a two-slot ring, or (TKV_T1_RESIDENT) a resident copy of every layer's T1 rows
+    A(dalloc(ctx, &ctx->stage, (c.t1_transport == TKV_T1_RESIDENT ? L : 2) * 2 * B * Hkv * S1 * d));
     const bool t2_host = c.t2_placement == TKV_T2_HOST;
     if (!t2_host) A(dalloc(ctx, &ctx->t2, L * 2 * B * Hkv * S2 * (d + 16)));
     else A(dalloc(ctx, &ctx->stage2, 2 * 2 * B * Hkv * S2 * (d + 16)));
@@ -739,7 +742,8 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
     a.q = (const __nv_bfloat16*)q;
     a.out = out;
     a.k0v0 = ctx->k0v0;
-    a.stage = ctx->stage + (size_t)slotr * 2 * ctx->B * ctx->Hkv * ctx->S1 * ctx->d;
+    a.stage = ctx->stage + (size_t)(ctx->cfg.t1_transport == TKV_T1_RESIDENT ? layer : slotr) * 2 * ctx->B *
+                               ctx->Hkv * ctx->S1 * ctx->d;
     if (ctx->t2_host) {
         a.t2 = ctx->stage2 + (size_t)slotr * 2 * ctx->B * ctx->Hkv * ctx->S2 * (ctx->d + 16);
         a.t2_layer = 0;
@@ -944,7 +948,9 @@ tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t
 tkv_status tkv_capture_begin(tkv_ctx* ctx) {
     CHECK_CTX();
     if (ctx->capturing || ctx->open_n != 0 || ctx->delta_max > 0 || ctx->profiling) return TKV_EINVAL;
-    if (ctx->cfg.t1_transport != TKV_T1_COPY_ENGINE && ctx->cfg.t1_transport != TKV_T1_SM_COPY) return TKV_EINVAL;
+    if (ctx->cfg.t1_transport != TKV_T1_COPY_ENGINE && ctx->cfg.t1_transport != TKV_T1_SM_COPY &&
+        ctx->cfg.t1_transport != TKV_T1_RESIDENT)
+        return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
     drop_graph(ctx);
     ctx->cap_saved.N = ctx->N;
@@ -1076,8 +1082,9 @@ tkv_status tkv_get_stats(tkv_ctx* ctx, tkv_stats* out) {
     // T0 rows, T2 records in HBM (or their two staged layers), and the two staged layers of T1
     const int64_t t2_in_hbm = ctx->t2_host ? (int64_t)2 * ctx->B * ctx->hw2 * 2 * ctx->Hkv * (ctx->d + 16)
                                            : s.tier_count[2] * r2;
+    const int64_t t1_layers = ctx->cfg.t1_transport == TKV_T1_RESIDENT ? ctx->L : 2;
     s.hbm_bytes_kv_resident = s.tier_count[0] * rb + t2_in_hbm +
-                              (int64_t)2 * ctx->B * ctx->hw1 * (int64_t)row_bytes_bf16(ctx);
+                              t1_layers * ctx->B * ctx->hw1 * (int64_t)row_bytes_bf16(ctx);
     s.kv_bytes_full_cache = (int64_t)ctx->N * ctx->B * rb;
     s.kernel_launches = ctx->launches;
     s.status = ctx->status;

@@ -238,6 +238,7 @@ struct MoveArgs {
     uint8_t* t2;
     __nv_bfloat16* h1;           // device view of the host T1 store
     __nv_bfloat16* h2m;          // device view of the host master store
+    __nv_bfloat16* t1_res;       // TKV_T1_RESIDENT: HBM copy of the T1 store [L][2][B][Hkv][S1][d], else null
     int layer_begin, layer_end;  // layers handled by this launch
     int L, B, Hkv, d, Nmax, S0, S1, S2;
     int max_count;
