@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     const int it0 = blockIdx.x * a.items_per_cta;
     const int it1 = min(total_items, it0 + a.items_per_cta);
     if (it0 >= it1) return;
-    const int g_first = it0 / IPG;
     uint8_t* ring = smem + C::off_ring + (size_t)warp * C::sz_warp_ring;
     float* p_s = reinterpret_cast<float*>(smem + C::off_p) + (size_t)warp * kRows * 2 * GP;
 
@@ -279,7 +278,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
             for (int c = 0; c < CPL / 2; ++c)
                 *reinterpret_cast<float2*>(cw + 16 + h * D + lane * CPL + 2 * c) = o[h][c];
         __syncthreads();
-        float* pout = a.part + ((size_t)blockIdx.x * a.part_segments + (g - g_first)) * PS;
+        // record (g, this CTA's rank among the CTAs that touch g)
+        const int c_lo = (g * IPG) / a.items_per_cta;
+        float* pout = a.part + ((size_t)g * a.part_per_group + (blockIdx.x - c_lo)) * PS;
         for (int i = tid; i < G * D + G; i += NT) {
             const int h = i < G * D ? i / D : i - G * D;
             float M = -INFINITY;
@@ -521,11 +522,8 @@ __global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) 
     float* m_s = fsm;
     float* l_s = fsm + ns * 8;
     float* f_s = fsm + 2 * ns * 8;
-    auto rec = [&](int sg) {
-        const int c = c_lo + sg;
-        const int seg = g - (c * ipc) / IPG;
-        return a.part + ((size_t)c * a.part_segments + seg) * PS;
-    };
+    const float* grec = a.part + (size_t)g * a.part_per_group * PS;
+    auto rec = [&](int sg) { return grec + (size_t)sg * PS; };
     // (1) loads: segment statistics, this thread's first batch of partial outputs, its logits
     for (int t = threadIdx.x; t < ns * 8; t += blockDim.x) {
         const int sg = t >> 3, h = t & 7;
@@ -624,7 +622,7 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
     // one alpha row per thread; enough blocks that every block holds at most 256 out elements
     const int rows = a.items_per_group * a.item_rows;
     const int blocks = std::max((rows + kCombineRows - 1) / kCombineRows, (G * D + kCombineRows - 1) / kCombineRows);
-    const int max_segs = (a.items_per_group + a.items_per_cta - 1) / a.items_per_cta + 1;
+    const int max_segs = a.part_per_group;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks, a.B * a.Hkv);
     cfg.blockDim = dim3(kCombineRows, 1, 1);
@@ -739,16 +737,18 @@ AttnPlan attention_plan(int G, int d, int B, int Hkv, int rmax, int resident) {
         p.items_per_cta = max_items;
         p.grid = (total + max_items - 1) / max_items;
     }
-    p.part_segments = (p.items_per_cta + p.items_per_group - 1) / p.items_per_group + 1;
+    p.part_per_group = (p.items_per_group + p.items_per_cta - 1) / p.items_per_cta + 1;
     p.smem = attention_smem_bytes(G, d, p.items_per_cta * p.item_rows);
     return p;
 }
 
 size_t attention_part_floats(int G, int d, int B, int Hkv, int Nmax, int resident) {
-    // grid * part_segments records: grid <= max(resident, items / 32), part_segments <= items_per_cta + 1
-    const size_t items = (size_t)B * Hkv * ((Nmax + 127) / 128);
-    const size_t grid = std::max<size_t>((size_t)resident, items / 32 + 1);
-    return (items + 2 * grid + 64) * (16 + (size_t)G * d);
+    // B * Hkv * part_per_group records, the largest over every retained count up to Nmax
+    // (the plan is constant over each 64-row bucket of counts)
+    size_t per_group = 0;
+    for (int r = 64; r < Nmax + 64; r += 64)
+        per_group = std::max(per_group, (size_t)attention_plan(G, d, B, Hkv, std::min(r, Nmax), resident).part_per_group);
+    return (size_t)B * Hkv * per_group * (16 + (size_t)G * d);
 }
 
 size_t attention_zs_floats(int G, int B, int Hkv, int Nmax) {

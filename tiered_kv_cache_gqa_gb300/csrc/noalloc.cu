@@ -140,7 +140,7 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
     a.items_per_group = plan.items_per_group;
     a.items_per_cta = plan.items_per_cta;
     a.grid = plan.grid;
-    a.part_segments = plan.part_segments;
+    a.part_per_group = plan.part_per_group;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)d));
     for (int l = 0; l < L; ++l) {
         a.layer = l;

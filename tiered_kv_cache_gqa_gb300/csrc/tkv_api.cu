@@ -766,7 +766,7 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
     a.items_per_group = plan.items_per_group;
     a.items_per_cta = plan.items_per_cta;
     a.grid = plan.grid;
-    a.part_segments = plan.part_segments;
+    a.part_per_group = plan.part_per_group;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)ctx->d));
     const bool timed = prof_open(ctx, 0, ctx->compute);
     CK(launch_attention(a, ctx->compute));

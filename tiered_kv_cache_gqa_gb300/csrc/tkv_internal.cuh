@@ -164,7 +164,7 @@ struct AttnArgs {
     const uint32_t* rl_loc;      // [B][Nmax]
     const int32_t* rl_count;     // [B]
     float* g;                    // [B][Hkv][Nmax] per-position alpha sums, running over the step's layers
-    float* part;                 // [grid][part_segments][16 + G*d] softmax partials per (CTA, group) (scratch)
+    float* part;                 // [B*Hkv][part_per_group][16 + G*d] softmax partials per (group, CTA of the group) (scratch)
     float* zs;                   // [B][Hkv][Nmax][GP] logits, log2-scaled (scratch)
     int32_t* err;                // status word (unused by kernels without device waits)
     int layer, L, B, Hq, Hkv, d, Nmax, S0, S1, S2;
@@ -172,13 +172,13 @@ struct AttnArgs {
     int item_rows;               // rows per item, a multiple of 128
     int items_per_cta;           // contiguous items per CTA
     int grid;                    // CTAs of the main kernel
-    int part_segments;           // partial records per CTA (groups a CTA's range can touch)
+    int part_per_group;          // partial records per group (CTAs whose ranges can touch a group)
     float qscale;                // log2(e) / sqrt(d)
 };
 
 // Launch geometry shared by the context path and the allocation-free path.
 struct AttnPlan {
-    int item_rows, items_per_group, items_per_cta, grid, part_segments;
+    int item_rows, items_per_group, items_per_cta, grid, part_per_group;
     size_t smem;
 };
 // Plans a launch for B sequences x Hkv heads with at most rmax retained rows.
