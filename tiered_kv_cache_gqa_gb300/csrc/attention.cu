@@ -61,7 +61,8 @@ struct AttnCfg {
     static constexpr size_t off_p = off_q + (size_t)G * D * 4;
     static constexpr size_t off_comb = off_p + (size_t)kAttnWarps * kRows * 2 * GP * 4;   // p as (p, p) pairs
     static constexpr size_t off_n = off_comb + (size_t)kAttnWarps * PS * 4;   // rows of each item
-    static constexpr size_t off_rl = off_n + (size_t)(kMaxWindowRows / 128) * 2 * 4;   // + decode-token flags
+    // per item: rows, decode-token flag, (sequence << 16 | KV head)
+    static constexpr size_t off_rl = off_n + (size_t)(kMaxWindowRows / 128) * 3 * 4;
 
     static size_t smem(int rl_rows) { return off_rl + (size_t)rl_rows * 4; }
 };
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     uint32_t* rl_s = reinterpret_cast<uint32_t*>(smem + C::off_rl);
     int* n_s = reinterpret_cast<int*>(smem + C::off_n);
     int* own_s = n_s + kMaxWindowRows / 128;
+    int* bk_s = n_s + 2 * (kMaxWindowRows / 128);
 
     // the combine kernel may be scheduled once every CTA of this grid has started
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         n_s[item - it0] = max(0, min(IT, R - j0));
         // the group's decode token (its last retained row) falls in this item
         own_s[item - it0] = (a.new_k != nullptr && R - 1 >= j0 && R - 1 < j0 + IT) ? 1 : 0;
+        bk_s[item - it0] = (b << 16) | (g % a.Hkv);
     }
     for (int item = it0; item < it1; ++item) {
         const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         const int jl = tile * kRows + lane;
         const uint8_t* src = nullptr;
         if (kv == 0) {
-            const int g = item / IPG, b = g / a.Hkv, kvh = g % a.Hkv;
+            const int bk = bk_s[item - it0], b = bk >> 16, kvh = bk & 0xFFFF;
             row_bytes = 0;
             bool fp8 = false;
             if (jl < n) {
