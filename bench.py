@@ -97,10 +97,11 @@ def describe(wl):
                *(100 * x for x in wl.ratios), wl.num_sinks, wl.window))
 
 
-def ncu_traffic(workload):
-    """DRAM bytes per attention launch from the committed ncu summary of this workload's
-    attention kernel, if it was captured from the attention source as it is now; else None.
-    The summary holds a line `traffic: <workload> <bytes per launch> <sha256 of attention.cu>`."""
+def ncu_traffic_ratio(workload):
+    """DRAM bytes (read + write) per attention launch over its algorithmic bytes, from the
+    committed ncu summary of this workload's attention kernel, if it was captured from the
+    attention source as it is now; else None.  The summary holds a line
+    `traffic_ratio: <workload> <ratio> <sha256 of attention.cu>`."""
     import hashlib
     src = os.path.join(ROOT, "tiered_kv_cache_gqa_gb300", "csrc", "attention.cu")
     try:
@@ -108,7 +109,7 @@ def ncu_traffic(workload):
         for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
             for line in open(os.path.join(ROOT, "profiles", name)):
                 f = line.strip().strip("`").split()
-                if len(f) == 4 and f[0] == "traffic:" and f[1] == workload and f[3] == digest:
+                if len(f) == 4 and f[0] == "traffic_ratio:" and f[1] == workload and f[3] == digest:
                     return float(f[2])
     except OSError:
         return None
@@ -507,6 +508,10 @@ def main():
         hbm_peak, peak_src = 6800.0, "fallback"
     pa, p1, pd = r["prof"]["attn"], r["prof"]["t1"], r["prof"]["delta"]
     KP_ = r["prof_steps"]
+    # DRAM bytes per launch: the ncu-measured ratio to the algorithmic bytes, scaled to this
+    # run's launches (traffic grows with the retained rows a launch reads)
+    ratio = ncu_traffic_ratio(args.workload) if not args.layers else None
+    traffic = ratio * pa["bytes"] / max(1, pa["count"]) if ratio else None
     achieved = pa["bytes"] / (pa["ms"] / 1e3) / 1e9 if pa["ms"] > 0 else 0.0
     st = r["stats"]
     t1_gbs = p1["bytes"] / (p1["ms"] / 1e3) / 1e9 if p1["ms"] > 0 else None
@@ -522,7 +527,7 @@ def main():
                    "l2": "flushed between timed steps (256 MB write); step working set %.0f MB"
                          % (st["kv_bytes_full_cache"] / 2 ** 20)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": ncu_traffic(args.workload) if not args.layers else None,
+                     "frac": achieved / hbm_peak, "traffic": traffic,
                      "kernel": "tkv::attn_kernel", "peak_source": peak_src,
                      "launches": pa["count"], "avg_launch_us": 1e3 * pa["ms"] / max(1, pa["count"]),
                      "bytes_per_launch": pa["bytes"] / max(1, pa["count"])},
