@@ -268,7 +268,7 @@ def run_gpu(args, rank, world):
     tkv.load()
     KP = prof_steps(args)
     wl = bench_workload(args.workload, args.warmup, args.steps + KP, args.t0, args.t3, args.layers)
-    wl = wl.with_(seed=wl.seed + 1000 * rank)
+    wl = wl.with_(seed=rank_seed(wl.seed, rank))
     L, B, Hq, Hkv, d = wl.num_layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     stream = torch.cuda.current_stream()
     t1_mode = {"ce": tkv.TKV_T1_COPY_ENGINE, "sm": tkv.TKV_T1_SM_COPY, "split": tkv.TKV_T1_SPLIT,
@@ -452,6 +452,31 @@ def run_gpu(args, rank, world):
             "prof_ms": prof_ms, "exposed": exposed}
 
 
+# ------------------------------------------------------------------ ranks
+# Replicas: every rank runs its own sequences (weak scaling, no data-path collective); only the
+# timing crosses ranks.
+def rank_seed(seed, rank):
+    """Seed of a rank's sequences: distinct sequences per rank."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(values):
+    """Element-wise max of a list of floats over every rank (gloo all-reduce); the input when
+    there is one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_tokens_per_s(batch, steps, world, max_ms):
+    """Tokens decoded by all ranks over the slowest rank's time."""
+    return batch * steps * world / (max_ms / 1e3)
+
+
 def main():
     args = parse()
     if args.oracle_worker:
@@ -488,18 +513,14 @@ def main():
     r = run_gpu(args, rank, world)
     total_ms = r["total_ms"]
     e2e_ms = r["e2e"]["ms"] if r["e2e"] else None
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, e2e_ms or 0.0], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), (float(t[1]) if e2e_ms is not None else None)
+    m = max_over_ranks([total_ms, e2e_ms or 0.0])
+    total_ms, e2e_ms = m[0], (m[1] if e2e_ms is not None else None)
     if rank != 0:
         return
     wl = r["wl"]
     K = args.steps
     tokens = wl.batch * K * world
-    value = tokens / (total_ms / 1e3)
+    value = whole_job_tokens_per_s(wl.batch, K, world, total_ms)
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
