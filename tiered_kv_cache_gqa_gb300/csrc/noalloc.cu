@@ -12,8 +12,9 @@
 // library holds until the process exits.
 //
 // Set-up: the first call on a device (with that device current) resolves the
-// arrays' device addresses with cudaGetSymbolAddress and checks which cluster
-// size fits; that first call should therefore come before any stream capture.
+// arrays' device addresses with cudaGetSymbolAddress and sets the attention
+// kernel's shared-memory limit; that first call should therefore come before
+// any stream capture.
 // Every call shares the arrays and leaves its contents in them; calls that
 // overlap on the GPU (for example on two streams) race on them.
 #include <cmath>
@@ -31,8 +32,8 @@ constexpr size_t kMaxAlphaFloats = kMaxGroupRows;     // per-row alpha sums over
 constexpr size_t kMaxTable = size_t(1) << 17;         // B*R        <= 131,072    (0.5 MiB)
 constexpr int kMaxBatch = 256;
 constexpr size_t kMaxZsFloats = kMaxGroupRows * 8;    // logits, 8 per row      (4 MiB)
-// softmax partials: (items + 2 * CTAs + 64) records of (16 + 8*128) floats, bounded for
-// B*Hkv*R <= 131,072 and up to 2 * 2048 CTAs
+// softmax partials: B*Hkv*part_per_group records of (16 + G*d) floats; this bound covers
+// B*Hkv*R <= 131,072 at the usual shapes, larger plans return TKV_ECAPACITY (checked per call)
 constexpr size_t kMaxPartFloats = (kMaxGroupRows / 128 + 2048 + 4096 + 64) * (16 + 8 * 128);   // ~29 MiB
 
 static __device__ __align__(256) float g_alpha_scratch[kMaxAlphaFloats];
