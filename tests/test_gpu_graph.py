@@ -23,9 +23,9 @@ WL = synth.Workload("graph", 3, 16, 4, 128, 2, prompt_len=16, prefill_len=600, d
 STEPS = 140
 
 
-def run(use_graph, t1_mode):
+def run(use_graph, t1_mode, t2_place=tkv.TKV_T2_HBM):
     gen = synth.Generator(WL)
-    ctx = tkv.TieredKV.for_workload(WL, t1_transport=t1_mode)
+    ctx = tkv.TieredKV.for_workload(WL, t1_transport=t1_mode, t2_placement=t2_place)
     prefill_both(ctx, None, gen)
     L, B, Hq, Hkv, d = WL.num_layers, WL.batch, WL.num_q_heads, WL.num_kv_heads, WL.head_dim
     out = torch.empty(L, B, Hq, d, device="cuda")
@@ -59,10 +59,13 @@ def run(use_graph, t1_mode):
     return res, replays, captures, ctx
 
 
-@pytest.mark.parametrize("t1_mode", [tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T1_SM_COPY, tkv.TKV_T1_RESIDENT])
-def test_replayed_steps_match_eager_steps_bitwise(t1_mode):
+@pytest.mark.parametrize("t1_mode,t2_place", [(tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T2_HBM),
+                                              (tkv.TKV_T1_SM_COPY, tkv.TKV_T2_HBM),
+                                              (tkv.TKV_T1_RESIDENT, tkv.TKV_T2_HBM),
+                                              (tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T2_HOST)])
+def test_replayed_steps_match_eager_steps_bitwise(t1_mode, t2_place):
     ref, _, _, _ = run(False, tkv.TKV_T1_COPY_ENGINE)
-    got, replays, captures, ctx = run(True, t1_mode)
+    got, replays, captures, ctx = run(True, t1_mode, t2_place)
     assert replays > 100 and captures >= 4          # geometry boundaries and re-tiers re-capture
     assert torch.equal(got[0], ref[0])
     assert np.array_equal(got[1], ref[1])
