@@ -273,7 +273,9 @@ def run_gpu(args, rank, world):
     stream = torch.cuda.current_stream()
     t1_mode = {"ce": tkv.TKV_T1_COPY_ENGINE, "sm": tkv.TKV_T1_SM_COPY, "split": tkv.TKV_T1_SPLIT,
                "multi": tkv.TKV_T1_MULTI_CE, "resident": tkv.TKV_T1_RESIDENT}[args.t1]
-    graph = args.mode == "graph"
+    # the multi-stream T1 transports are not capturable: their steps run eagerly
+    graph = args.mode == "graph" and args.t1 not in ("split", "multi")
+    args.steps_as = "graph" if graph else "eager"
     t2_place = tkv.TKV_T2_HOST if args.t2 == "host" else tkv.TKV_T2_HBM
     gen = synth.Generator(wl, device="cuda")
     n_steps = PRE_STEPS + args.warmup + args.steps + KP
@@ -544,7 +546,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": describe(wl), "global_batch": wl.batch * world,
                    "seq_len": TARGET_N[args.workload], "parallelism": "replicas (sequence shards)",
-                   "t1_transport": args.t1, "t2_placement": args.t2, "steps_as": args.mode,
+                   "t1_transport": args.t1, "t2_placement": args.t2, "steps_as": getattr(args, "steps_as", args.mode),
                    "l2": "flushed between timed steps (256 MB write); step working set %.0f MB"
                          % (st["kv_bytes_full_cache"] / 2 ** 20)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
