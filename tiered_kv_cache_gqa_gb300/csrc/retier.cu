@@ -340,8 +340,8 @@ __global__ void __launch_bounds__(128) moves_kernel(const MoveArgs a) {
             const __nv_bfloat16* sp;
             if (kind == MV_T0_T1 || kind == MV_T0_T2)
                 sp = a.k0v0 + row_index(layer, kv, b, h, src, a.B, a.Hkv, a.S0) * D;
-            else if (kind == MV_T1_T2 || kind == MV_T1_T0)
-                sp = a.h1 + row_index(layer, kv, b, h, src, a.B, a.Hkv, a.S1) * D;
+            else if (kind == MV_T1_T2 || kind == MV_T1_T0)   // the resident HBM copy when there is one
+                sp = (a.t1_res ? a.t1_res : a.h1) + row_index(layer, kv, b, h, src, a.B, a.Hkv, a.S1) * D;
             else
                 sp = a.h2m + row_index(layer, kv, b, h, src, a.B, a.Hkv, a.S2) * D;
             w[it] = *reinterpret_cast<const uint4*>(sp + sub * 8);
