@@ -273,8 +273,8 @@ def run_gpu(args, rank, world):
     stream = torch.cuda.current_stream()
     t1_mode = {"ce": tkv.TKV_T1_COPY_ENGINE, "sm": tkv.TKV_T1_SM_COPY, "split": tkv.TKV_T1_SPLIT,
                "multi": tkv.TKV_T1_MULTI_CE, "resident": tkv.TKV_T1_RESIDENT}[args.t1]
-    # the multi-stream T1 transports are not capturable: their steps run eagerly
-    graph = args.mode == "graph" and args.t1 not in ("split", "multi")
+    # the split T1 transport is not capturable: its steps run eagerly
+    graph = args.mode == "graph" and args.t1 != "split"
     args.steps_as = "graph" if graph else "eager"
     t2_place = tkv.TKV_T2_HOST if args.t2 == "host" else tkv.TKV_T2_HBM
     gen = synth.Generator(wl, device="cuda")

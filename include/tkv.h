@@ -293,8 +293,8 @@ tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, float* out, f
  * serving loop takes the host-side cost of the per-layer calls (and the gaps
  * between launches) off a decode step.
  * tkv_capture_begin: between decode steps, with no delta prefetch pending
- * (i.e. not on the first step after a re-tier), profiling off and the T1
- * transport TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY or TKV_T1_RESIDENT.  The caller then makes one
+ * (i.e. not on the first step after a re-tier), profiling off and any T1
+ * transport but TKV_T1_SPLIT.  The caller then makes one
  * decode step's calls (tkv_append / tkv_prefetch / tkv_decode_step for every
  * layer) as usual: they are recorded into a graph, on an internal stream, and
  * nothing runs.  tkv_capture_end instantiates the graph, puts the context back

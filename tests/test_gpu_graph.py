@@ -62,6 +62,7 @@ def run(use_graph, t1_mode, t2_place=tkv.TKV_T2_HBM):
 @pytest.mark.parametrize("t1_mode,t2_place", [(tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T2_HBM),
                                               (tkv.TKV_T1_SM_COPY, tkv.TKV_T2_HBM),
                                               (tkv.TKV_T1_RESIDENT, tkv.TKV_T2_HBM),
+                                              (tkv.TKV_T1_MULTI_CE, tkv.TKV_T2_HBM),
                                               (tkv.TKV_T1_COPY_ENGINE, tkv.TKV_T2_HOST)])
 def test_replayed_steps_match_eager_steps_bitwise(t1_mode, t2_place):
     ref, _, _, _ = run(False, tkv.TKV_T1_COPY_ENGINE)

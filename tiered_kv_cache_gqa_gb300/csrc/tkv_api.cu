@@ -80,6 +80,7 @@ struct tkv_ctx {
     cudaStream_t cap_stream = nullptr, cap_saved_compute = nullptr;
     cudaEvent_t ev_fork = nullptr;        // recorded on the capture stream when the capture opens
     bool copy_joined = false;             // the copy stream has joined the capture
+    bool copyx_joined[3] = {false, false, false};   // and so have the helper copy streams
     bool attn_in_capture[2] = {false, false};
     int cap_rows = 0;                     // rows per group the captured launch geometry covers
     struct Saved {
@@ -405,8 +406,17 @@ tkv_status issue_prefetch(tkv_ctx* ctx, int layer) {
                 const int r0 = height * k / parts, r1 = height * (k + 1) / parts;
                 if (r1 <= r0) continue;
                 cudaStream_t hs = ctx->copyx[k - 1];
-                CK(cudaStreamWaitEvent(hs, ctx->ev_attn[slotr], 0));
-                CK(cudaStreamWaitEvent(hs, ctx->ev_retier, 0));
+                if (ctx->capturing) {
+                    // helper streams join the capture like the copy stream
+                    if (!ctx->copyx_joined[k - 1]) {
+                        CK(cudaStreamWaitEvent(hs, ctx->ev_fork, 0));
+                        ctx->copyx_joined[k - 1] = true;
+                    }
+                    if (ctx->attn_in_capture[slotr]) CK(cudaStreamWaitEvent(hs, ctx->ev_attn[slotr], 0));
+                } else {
+                    CK(cudaStreamWaitEvent(hs, ctx->ev_attn[slotr], 0));
+                    CK(cudaStreamWaitEvent(hs, ctx->ev_retier, 0));
+                }
                 CK(cudaMemcpy2DAsync((uint8_t*)dst + (size_t)r0 * pitch, pitch, (const uint8_t*)src + (size_t)r0 * pitch,
                                      pitch, width, r1 - r0, cudaMemcpyHostToDevice, hs));
                 CK(cudaEventRecord(ctx->ev_join[k - 1], hs));
@@ -948,9 +958,7 @@ tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t
 tkv_status tkv_capture_begin(tkv_ctx* ctx) {
     CHECK_CTX();
     if (ctx->capturing || ctx->open_n != 0 || ctx->delta_max > 0 || ctx->profiling) return TKV_EINVAL;
-    if (ctx->cfg.t1_transport != TKV_T1_COPY_ENGINE && ctx->cfg.t1_transport != TKV_T1_SM_COPY &&
-        ctx->cfg.t1_transport != TKV_T1_RESIDENT)
-        return TKV_EINVAL;
+    if (ctx->cfg.t1_transport == TKV_T1_SPLIT) return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
     drop_graph(ctx);
     ctx->cap_saved.N = ctx->N;
@@ -971,6 +979,7 @@ tkv_status tkv_capture_begin(tkv_ctx* ctx) {
     ctx->compute = ctx->cap_stream;
     ctx->capturing = true;
     ctx->copy_joined = false;
+    for (bool& j : ctx->copyx_joined) j = false;
     ctx->attn_in_capture[0] = ctx->attn_in_capture[1] = false;
     ctx->cap_rows = 0;
     return TKV_OK;
