@@ -8,9 +8,12 @@
  *   T0  HBM, full precision (bf16)          -- protected tokens and the most
  *                                              important reasoning tokens
  *   T1  pinned host DDR, full precision     -- fetched back into HBM before
- *                                              each attention step
+ *                                              each attention step (or read
+ *                                              from an HBM copy the re-tier
+ *                                              keeps: TKV_T1_RESIDENT)
  *   T2  8-bit (FP8-E4M3, one fp32 scale per token, layer and KV head, for K
- *       and for V), kept in HBM and dequantised inside the attention load
+ *       and for V), kept in HBM or in pinned host memory (TKV_T2_HOST) and
+ *       dequantised inside the attention load
  *   T3  evicted (dropped from every store)
  *
  * ranked by the cumulative attention score
@@ -105,8 +108,9 @@ typedef struct {
     int32_t t0_capacity;      /* HBM T0 slots per sequence; 0 = max_tokens */
     int32_t t1_capacity;      /* pinned-host T1 slots per sequence (and HBM staging rows); 0 = max_tokens */
     int32_t t2_capacity;      /* T2 slots per sequence; 0 = max_tokens if ratio_t2 > 0, else 0 */
-    int32_t t1_transport;     /* how the per-layer T1 rows reach HBM staging: TKV_T1_COPY_ENGINE,
-                                 TKV_T1_SM_COPY or TKV_T1_SPLIT (see below) */
+    int32_t t1_transport;     /* how T1 rows reach the attention kernel: TKV_T1_COPY_ENGINE,
+                                 TKV_T1_SM_COPY, TKV_T1_SPLIT, TKV_T1_MULTI_CE or TKV_T1_RESIDENT
+                                 (see above) */
     int32_t device;           /* CUDA device ordinal */
     void* compute_stream;     /* cudaStream_t for attention, append, fold, re-tier; NULL = create a
                                  non-blocking one (then order the caller's work with tkv_sync);
@@ -131,7 +135,8 @@ typedef struct {
     int64_t d2h_bytes_writeback;   /* cumulative bytes written back to the host stores */
     int64_t hbm_bytes_allocated;   /* device bytes held by the context */
     int64_t host_bytes_allocated;  /* pinned host bytes held by the context */
-    int64_t hbm_bytes_kv_resident; /* KV bytes in HBM now: T0 rows + T2 rows + T1 staging */
+    int64_t hbm_bytes_kv_resident; /* KV bytes in HBM now: T0 rows + T2 rows (or their two staged layers)
+                                      + T1 staging (or the resident T1 copy) */
     int64_t kv_bytes_full_cache;   /* bf16 KV bytes of all N positions (no tiering) */
     int64_t kernel_launches;       /* kernels this context has launched (all kinds) */
     int32_t status;                /* tkv_status of the context */
