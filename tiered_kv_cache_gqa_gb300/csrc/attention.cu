@@ -15,24 +15,29 @@
 // w + 4.  Each warp streams, item after item, the K rows and then the V rows
 // of its tiles through its own two-stage shared-memory ring with 16-byte
 // cp.async (16 lanes per 256-byte row, every row fetched from its home: T0
-// pool, T1 staging or T2 pool), so the next tile -- possibly of the next item --
-// is in flight while the current one is computed.  The only waits are
-// cp.async.wait_group and CTA barriers; there are no spin loops.
+// pool, T1 staging or T2 records; the group's decode token from the caller's
+// k/v, stored into its T0 slot from the ring), so the next tile -- possibly
+// of the next item -- is in flight while the current one is computed.  The
+// only waits are cp.async.wait_group and CTA barriers; there are no spin loops.
 //   K tile:  lane = row; z_h = q'_h . k for the G query heads of the group,
 //            q' = q * log2(e)/sqrt(d) in shared memory (broadcast reads),
 //            packed f32x2 FMAs; T2 rows: z = scale * (q' . code values).
-//   stats:   per warp and item, m_h = max z, p = 2^(z - m_h), l_h = sum p;
-//            z goes to a global scratch for the alpha sums.
+//   stats:   per warp and group, online over its tiles: m_h = max z,
+//            p = 2^(z - m_h), l_h = sum p; z goes to a global scratch for the
+//            alpha sums.
 //   V tile:  the warp walks the tile's rows, lane = 4 (or 2) columns,
 //            O_h += p * v.
-//   item end: the four warps' (m, l, O) are merged in shared memory (fixed
-//            order) into the item's partial, written to global scratch.
-// The combine kernel then merges a group's item partials in item order into
-// `out`, and writes per position g = sum_h 2^(z_h - M_h) / L_h (the sum over the
-// group's query heads of alpha).  Item boundaries, the CTA ranges and every
-// reduction order depend only on the retained counts, never on which tier a
-// row sits in, so a row read from T0 or from the T1 staging ring gives
-// bit-identical results.  No atomics touch `out` or `g`.
+//   group end: the four warps' (m, l, O) are merged in shared memory (fixed
+//            order) into the CTA's partial for the group, stored at (group,
+//            the CTA's rank among the CTAs that touch the group).
+// The combine kernel then merges a group's partials in CTA order into `out`,
+// and adds per position g = sum_h 2^(z_h - M_h) / L_h (the sum over the group's
+// query heads of alpha) to a running sum over the step's layers.  Item
+// boundaries, the CTA ranges and every reduction order depend only on the
+// retained counts, never on which tier a row sits in, so a row read from T0 or
+// from T1 staging gives bit-identical results.  No atomics touch `out` or `g`.
+// Launches in which every warp streams at most two tiles use a compact
+// instantiation (partly unrolled loops, same arithmetic in the same order).
 #include <algorithm>
 #include <cmath>
 
