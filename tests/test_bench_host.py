@@ -56,3 +56,17 @@ def test_clock_samples_are_filtered_to_the_timed_window(tmp_path, monkeypatch):
     assert out["samples"] == 2
     assert out["sm_mhz"] == 2060.0 and out["sm_max_mhz"] == 2070.0
     assert out["reasons"] == ["sw_thermal_slowdown"]
+
+
+def test_reference_arm_runs_on_cpu_and_prints_its_line():
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT,
+                       env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["higher_is_better"] is True
