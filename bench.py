@@ -543,8 +543,9 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": describe(wl), "global_batch": wl.batch * world,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": describe(wl), "inputs": "bf16 K/V/q (T2 rows FP8-E4M3), fp32 arithmetic",
+                   "global_batch": wl.batch * world,
                    "seq_len": TARGET_N[args.workload], "parallelism": "replicas (sequence shards)",
                    "t1_transport": args.t1, "t2_placement": args.t2, "steps_as": getattr(args, "steps_as", args.mode),
                    "l2": "flushed between timed steps (256 MB write); step working set %.0f MB"
