@@ -179,7 +179,9 @@ tkv_status tkv_append(tkv_ctx* ctx, int32_t layer, const void* k, const void* v,
  * before each attention step; "System implementation": asynchronous delta
  * prefetch of newly promoted tokens only).  Call it for layer l+1 before
  * tkv_decode_step(l) so the copy overlaps layer l's attention; if it was not
- * called, tkv_decode_step(layer) issues it itself.
+ * called, tkv_decode_step(layer) issues it itself.  Layers may be prefetched
+ * in any order (at most two layers ahead of the attention): each layer's
+ * delta is enqueued, once, before that layer's fetch completes.
  * Errors: TKV_EINVAL (layer out of range, or called twice for one layer in
  * one step). */
 tkv_status tkv_prefetch(tkv_ctx* ctx, int32_t layer);
@@ -224,8 +226,9 @@ tkv_status tkv_get_tiers(tkv_ctx* ctx, uint8_t* dst_host);
 
 /* Moves every position to the given tier (test hook, e.g. for Proposition 1:
  * same T3 set, different T0/T1 splits): src [B][N] uint8.  Data moves exactly
- * as in tkv_retier.  An evicted position cannot be given back a tier
- * (TKV_EINVAL, nothing changes).  Synchronises. */
+ * as in tkv_retier.  An evicted position cannot be given back a tier, and a
+ * protected position (sinks, prompt, recent window at the current N) cannot be
+ * evicted (TKV_EINVAL, nothing changes).  Synchronises. */
 tkv_status tkv_set_tiers(tkv_ctx* ctx, const uint8_t* src_host);
 
 /* Inspection hook: copies the stored K and V rows of one position of one
@@ -314,6 +317,23 @@ tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, float* out, f
 tkv_status tkv_capture_begin(tkv_ctx* ctx);
 tkv_status tkv_capture_end(tkv_ctx* ctx, int32_t* steps_valid);
 tkv_status tkv_replay(tkv_ctx* ctx);
+
+/* Measurement hook (no counterpart on the pages, which quote PCIe Gen5 x16 for
+ * their prototype's host link): the bandwidth of this device's host link as
+ * seen by the two ways the library moves host rows.  Allocates `bytes` of
+ * pinned mapped host memory and of device memory, times the best of three
+ * passes of each kind with CUDA events on a stream of its own, frees both and
+ * synchronises:
+ *   h2d_ce_gbs  one cudaMemcpyAsync, pinned host -> device (the copy engine
+ *               that carries the per-layer T1 stream);
+ *   h2d_sm_gbs  the library's copy kernel loading the mapped host buffer
+ *               (zero-copy; the path the delta prefetch and TKV_T1_SM_COPY use);
+ *   d2h_ce_gbs  one cudaMemcpyAsync, device -> pinned host.
+ * GB/s = 1e9 bytes per second.  Any output pointer may be NULL.
+ * Errors: TKV_EINVAL (bytes < 1 MiB or not a multiple of 16, device < 0),
+ * TKV_ENOMEM, TKV_ECUDA. */
+tkv_status tkv_measure_host_link(int32_t device, int64_t bytes, double* h2d_ce_gbs, double* h2d_sm_gbs,
+                                 double* d2h_ce_gbs);
 
 /* Waits for all enqueued work and reports any device-side status word. */
 tkv_status tkv_sync(tkv_ctx* ctx);

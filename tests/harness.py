@@ -30,12 +30,16 @@ def prefill_both(ctx, sess, gen, n=None):
     return K, V
 
 
-def gpu_step(ctx, q, k, v, out):
-    """One decode step through the C ABI, in the canonical call order."""
+def gpu_step(ctx, q, k, v, out, order="canonical"):
+    """One decode step through the C ABI.
+
+    order="canonical": append(l); prefetch(0) when l == 0; prefetch(l+1); decode_step(l).
+    order="ahead": layer 0 is never prefetched explicitly (decode_step(0) issues it, after
+    prefetch(1) has run): append(l); prefetch(l+1); decode_step(l)."""
     L = q.shape[0]
     for l in range(L):
         ctx.append(l, k[l], v[l], 1)
-        if l == 0:
+        if l == 0 and order == "canonical":
             ctx.prefetch(0)
         if l + 1 < L:
             ctx.prefetch(l + 1)
@@ -49,11 +53,12 @@ def check_scores(s_gpu, s_ref):
         float(err.max()), float(bound[np.argmax(err - bound)]))
 
 
-def lockstep(wl, steps, device="cpu", check_out=True, **ctx_kw):
+def lockstep(wl, steps, device="cpu", check_out=True, order="canonical", on_retier=None, **ctx_kw):
     """Runs `steps` decode steps on both sides; re-tier every wl.delta steps.
 
     The re-tier is checked bit-exactly by feeding the GPU's fp32 scores to the
     oracle's tier assignment; both sides then continue from the same tiers.
+    `on_retier(t, ctx)` is called after each re-tier.
     Returns (ctx, sess, worst output error)."""
     gen = synth.Generator(wl, device=device)
     ctx = tkv.TieredKV.for_workload(wl, **ctx_kw)
@@ -64,7 +69,7 @@ def lockstep(wl, steps, device="cpu", check_out=True, **ctx_kw):
     worst = 0.0
     for t in range(1, steps + 1):
         q, k, v = gen.decode_step(t)
-        gpu_step(ctx, q.cuda(), k.cuda(), v.cuda(), out)
+        gpu_step(ctx, q.cuda(), k.cuda(), v.cuda(), out, order=order)
         ref = sess.step(q.float().numpy(), k.float().numpy(), v.float().numpy(), auto_retier=False)
         if check_out:
             err = float(np.abs(out.cpu().numpy().astype(np.float64) - ref).max())
@@ -79,4 +84,6 @@ def lockstep(wl, steps, device="cpu", check_out=True, **ctx_kw):
             assert np.array_equal(t_gpu, want), "step %d: tiers differ at %s" % (
                 t, np.argwhere(t_gpu != want)[:10].tolist())
             sess.apply_tiers(want)
+            if on_retier is not None:
+                on_retier(t, ctx)
     return ctx, sess, worst

@@ -231,10 +231,44 @@ def test_call_order_and_capacity_errors_leave_context_usable():
     ctx.sync()
 
 
+def test_prefetch_ahead_of_layer_0_applies_every_layers_delta():
+    """Layers prefetched out of order -- prefetch(1) before decode_step(0), layer 0 never
+    prefetched explicitly -- across re-tiers that promote rows: every layer still reads its
+    promoted rows from T0 (lockstep with the oracle on out, s and tiers every step)."""
+    wl = synth.Workload("ahead", 3, 16, 4, 128, 2, prompt_len=16, prefill_len=600, decode_steps=48,
+                        window=16, delta=16, ratios=(0.3, 0.6, 0.05, 0.05), seed=12)
+    promoted = []
+    ctx, sess, worst = lockstep(wl, 48, order="ahead",
+                                on_retier=lambda t, c: promoted.append(c.stats()["last_promoted"]))
+    assert len(promoted) == 3 and sum(promoted[1:]) > 0
+
+
+def test_set_tiers_refuses_to_evict_a_protected_position():
+    """Sinks, prompt and recent window are never evicted: tkv_set_tiers returns EINVAL and
+    changes nothing; an unprotected position can be evicted."""
+    ctx = tkv.TieredKV(num_layers=1, num_q_heads=4, num_kv_heads=2, head_dim=64, batch=1,
+                       max_tokens=32, prompt_len=6, num_sinks=2, recent_window=4,
+                       ratios=(0.5, 0.5, 0.0, 0.0))
+    k = torch.zeros(1, 20, 2, 64, dtype=torch.bfloat16, device="cuda")
+    ctx.append(0, k, k, 20)
+    for pos in (0, 5, 16, 19):                      # sink, prompt, window (N - W = 16), last
+        bad = np.zeros((1, 20), dtype=np.uint8)
+        bad[0, pos] = 3
+        assert tkv.tkv_set_tiers(ctx.ctx, bad) == tkv.TKV_EINVAL, pos
+        assert (ctx.tiers() == 0).all()
+    ok = np.zeros((1, 20), dtype=np.uint8)
+    ok[0, 10] = 3
+    ctx.set_tiers(ok)
+    assert np.array_equal(ctx.tiers(), ok)
+    assert ctx.stats()["status"] == tkv.TKV_OK
+
+
 def test_t1_transports_are_bitwise_identical():
     """Copy engine, SM copy kernel, the split of both, four copy streams and the HBM-resident
     copy kept by the re-tier put the same bytes in the rows the kernel reads: outputs and scores
-    are bit-identical, and match the oracle.  The resident copy streams nothing per step."""
+    are bit-identical across the five transports (the copy-engine transport is the one the
+    lockstep tests compare with the oracle; the resident copy has its own lockstep test below).
+    The resident copy streams nothing per step."""
     wl = synth.Workload("t1x", 3, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
                         window=16, ratios=(0.3, 0.6, 0.05, 0.05), seed=8)
     outs = []
@@ -257,6 +291,20 @@ def test_t1_transports_are_bitwise_identical():
     for o, s, _ in outs[1:]:
         assert torch.equal(o, outs[0][0])
         assert np.array_equal(s, outs[0][1])
+
+
+def test_resident_t1_lockstep_with_the_oracle():
+    """TKV_T1_RESIDENT (the HBM copy of T1 kept by the re-tier's moves) in lockstep with the
+    fp64 oracle: out, s and tiers every step, across two re-tiers that demote, promote,
+    quantise and evict."""
+    wl = synth.Workload("t1res", 3, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
+                        window=16, delta=32, ratios=(0.3, 0.55, 0.1, 0.05), outlier_rate=0.01, seed=13)
+    promoted = []
+    ctx, sess, worst = lockstep(wl, 70, t1_transport=tkv.TKV_T1_RESIDENT,
+                                on_retier=lambda t, c: promoted.append(c.stats()["last_promoted"]))
+    st = ctx.stats()
+    assert st["h2d_bytes_t1_stream"] == 0 and st["retiers"] == 2 and promoted[1] > 0
+    assert st["tier_count"][1] > 0 and st["tier_count"][2] > 0 and st["tier_count"][3] > 0
 
 
 def test_t2_on_host_matches_t2_in_hbm_bitwise_and_the_oracle():

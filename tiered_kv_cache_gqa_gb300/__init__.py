@@ -27,7 +27,7 @@ EXPORTS = ("tkv_create", "tkv_destroy", "tkv_append", "tkv_prefetch", "tkv_decod
            "tkv_retier", "tkv_get_scores", "tkv_set_scores", "tkv_get_tiers", "tkv_set_tiers",
            "tkv_get_row", "tkv_profile_begin", "tkv_profile_end", "tkv_sync", "tkv_get_stats",
            "tkv_status_string", "tkv_decode_dense_noalloc", "tkv_capture_begin", "tkv_capture_end",
-           "tkv_replay")
+           "tkv_replay", "tkv_measure_host_link")
 
 
 class TkvUnavailable(RuntimeError):
@@ -119,6 +119,8 @@ def load():
     lib.tkv_capture_end.argtypes = [vp, ctypes.POINTER(i32)]
     lib.tkv_replay.argtypes = [vp]
     lib.tkv_sync.argtypes = [vp]
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.tkv_measure_host_link.argtypes = [i32, ctypes.c_int64, dp, dp, dp]
     lib.tkv_get_stats.argtypes = [vp, ctypes.POINTER(Stats)]
     lib.tkv_status_string.argtypes = [st]
     lib.tkv_status_string.restype = ctypes.c_char_p
@@ -235,6 +237,13 @@ def tkv_decode_dense_noalloc(q, kv, out, s, num_layers, batch, num_q_heads, num_
     return load().tkv_decode_dense_noalloc(_ptr(q), _ptr(kv), _ptr(out), _ptr(s), int(num_layers),
                                            int(batch), int(num_q_heads), int(num_kv_heads),
                                            int(head_dim), int(num_positions), ctypes.c_void_p(stream))
+
+
+def tkv_measure_host_link(device, nbytes):
+    """Returns (status, {"h2d_ce_gbs", "h2d_sm_gbs", "d2h_ce_gbs"}) (see include/tkv.h)."""
+    v = [ctypes.c_double(0.0) for _ in range(3)]
+    rc = load().tkv_measure_host_link(int(device), int(nbytes), *(ctypes.byref(x) for x in v))
+    return rc, {"h2d_ce_gbs": v[0].value, "h2d_sm_gbs": v[1].value, "d2h_ce_gbs": v[2].value}
 
 
 def tkv_sync(ctx):

@@ -153,6 +153,12 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
         }
     }
     const float inv = (float)(1.0 / ((double)L * (double)Hq));
+    // The fold maps retained index j to its position through an int32 table.  Here every
+    // entry of the retained-index table is make_loc(0, j): tier bits 0 and slot j, which is
+    // the integer j itself, so the same words serve as that position table.
+    static_assert(sizeof(uint32_t) == sizeof(int32_t) && make_loc(0, 1) == 1u &&
+                      make_loc(0, (int)(kMaxTable - 1)) == (uint32_t)(kMaxTable - 1),
+                  "a T0 location word equals its slot, so the index table doubles as positions");
     if (launch_fold(sc->alpha, (const int32_t*)sc->index, sc->count, s, B, Hkv, R, R, inv, st) !=
         cudaSuccess) {
         (void)cudaGetLastError();

@@ -94,7 +94,7 @@ struct tkv_ctx {
     int64_t graph_launches = 0, graph_t1_bytes = 0, graph_t2_bytes = 0;
     int delta_max = 0;                 // pending delta moves (max over sequences), 0 = none
     int delta_chunk = 1;               // layers per delta launch (about 1 MB of rows per launch)
-    int delta_next = 0;                // first layer whose delta is not enqueued yet
+    std::vector<char> delta_done;      // per layer: its delta is enqueued (valid while delta_max > 0)
 
     int resident = 1;                  // attention CTAs resident on the device at once
     int last_splits = 0;
@@ -275,13 +275,32 @@ tkv_status enqueue_delta(tkv_ctx* ctx, int l0, int l1, cudaStream_t st) {
     return TKV_OK;
 }
 
+// Enqueues the delta of every layer in [l0, l1) not enqueued yet, as launches over runs of
+// consecutive such layers of at most `chunk` layers, and marks those layers done.
+tkv_status enqueue_delta_range(tkv_ctx* ctx, int l0, int l1, int chunk, cudaStream_t st) {
+    int l = l0;
+    while (l < l1) {
+        if (ctx->delta_done[l]) {
+            ++l;
+            continue;
+        }
+        int e = l;
+        while (e < l1 && e - l < chunk && !ctx->delta_done[e]) ++e;
+        tkv_status r = enqueue_delta(ctx, l, e, st);
+        if (r != TKV_OK) return r;
+        for (int k = l; k < e; ++k) ctx->delta_done[k] = 1;
+        l = e;
+    }
+    return TKV_OK;
+}
+
 // Re-tier core shared by tkv_retier (ranked) and tkv_set_tiers (forced).
 tkv_status run_retier(tkv_ctx* ctx, bool forced) {
     const int N = ctx->N, B = ctx->B;
     drop_graph(ctx);
     // a delta left by an earlier re-tier that no decode step has consumed yet
     if (ctx->delta_max > 0) {
-        tkv_status r = enqueue_delta(ctx, 0, ctx->L, ctx->compute);
+        tkv_status r = enqueue_delta_range(ctx, 0, ctx->L, ctx->L, ctx->compute);
         if (r != TKV_OK) return r;
         ctx->delta_max = 0;
     }
@@ -361,7 +380,7 @@ tkv_status run_retier(tkv_ctx* ctx, bool forced) {
         const int64_t per_layer = rows * (int64_t)row_bytes_bf16(ctx);
         const int64_t want = int64_t(1) << 20;
         ctx->delta_chunk = (int)std::min<int64_t>(ctx->L, std::max<int64_t>(1, per_layer > 0 ? (want + per_layer - 1) / per_layer : 1));
-        ctx->delta_next = 0;
+        std::fill(ctx->delta_done.begin(), ctx->delta_done.end(), 0);
     }
 
     const int64_t rb = (int64_t)row_bytes_bf16(ctx) * ctx->L;
@@ -467,12 +486,12 @@ t1_done:
         if (timed) prof_close(ctx, 1, ctx->copy, (double)(width * height));
         ctx->st.h2d_bytes_t2_stream += (int64_t)(width * height);
     }
-    if (ctx->delta_max > 0 && layer >= ctx->delta_next) {
-        // this layer's delta and the next ones' of its chunk, before this layer's T1 event
-        const int l1 = std::min(ctx->L, layer + ctx->delta_chunk);
-        tkv_status r = enqueue_delta(ctx, layer, l1, ctx->copy);
+    if (ctx->delta_max > 0 && !ctx->delta_done[layer]) {
+        // this layer's delta and that of the following layers of its chunk whose delta is
+        // not enqueued yet, before this layer's T1 event (layers may be prefetched in any order)
+        tkv_status r = enqueue_delta_range(ctx, layer, std::min(ctx->L, layer + ctx->delta_chunk),
+                                           ctx->delta_chunk, ctx->copy);
         if (r != TKV_OK) return r;
-        ctx->delta_next = l1;
     }
     CK(cudaEventRecord(ctx->ev_t1[slotr], ctx->copy));
     ctx->prefetched[layer] = 1;
@@ -656,6 +675,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     for (int t = 0; t < 4; ++t) ctx->count[t].assign(B, 0);
     ctx->R.assign(B, 0);
     ctx->prefetched.assign(L, 0);
+    ctx->delta_done.assign(L, 0);
     ctx->pend_k.assign(L, nullptr);
     ctx->pend_v.assign(L, nullptr);
     *out = ctx;
@@ -866,6 +886,11 @@ tkv_status tkv_set_tiers(tkv_ctx* ctx, const uint8_t* src) {
     for (size_t i = 0; i < cur.size(); ++i) {
         if (src[i] > 3) return TKV_EINVAL;
         if (cur[i] == 3 && src[i] != 3) return TKV_EINVAL;
+        // protected positions (sinks, prompt, recent window at the current N) are never evicted
+        const int pos = (int)(i % (size_t)N);
+        if (src[i] == 3 && (pos < ctx->cfg.num_sinks || pos < ctx->cfg.prompt_len ||
+                            pos >= N - ctx->cfg.recent_window))
+            return TKV_EINVAL;
     }
     if (N > 0)
         CK(cudaMemcpy2D(ctx->forced, ctx->Nmax, src, N, N, B, cudaMemcpyHostToDevice));
@@ -1071,6 +1096,64 @@ tkv_status tkv_sync(tkv_ctx* ctx) {
     CK(cudaStreamSynchronize(ctx->copy));
     CK(cudaStreamSynchronize(ctx->compute));
     return read_device_status(ctx);
+}
+
+tkv_status tkv_measure_host_link(int32_t device, int64_t bytes, double* h2d_ce_gbs, double* h2d_sm_gbs,
+                                 double* d2h_ce_gbs) {
+    if (bytes < (1 << 20) || (bytes & 15) || device < 0) return TKV_EINVAL;
+    DeviceGuard guard(device);
+    if (cudaSetDevice(device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TKV_ECUDA;
+    }
+    const size_t n = (size_t)bytes;
+    void *h = nullptr, *dh = nullptr, *dbuf = nullptr;
+    cudaStream_t st = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    tkv_status rc = TKV_OK;
+    double best[3] = {0.0, 0.0, 0.0};   // GB/s: H2D copy engine, H2D SM loads, D2H copy engine
+    if (cudaHostAlloc(&h, n, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess ||
+        cudaMalloc(&dbuf, n) != cudaSuccess) {
+        rc = TKV_ENOMEM;
+    } else if (cudaHostGetDevicePointer(&dh, h, 0) != cudaSuccess ||
+               cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+               cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        rc = TKV_ECUDA;
+    } else {
+        std::memset(h, 0x5a, n);
+        // one untimed pass of each kind, then the best of three timed passes
+        for (int rep = 0; rep < 4 && rc == TKV_OK; ++rep) {
+            for (int kind = 0; kind < 3; ++kind) {
+                cudaError_t e = cudaEventRecord(e0, st);
+                if (e == cudaSuccess) {
+                    if (kind == 0) e = cudaMemcpyAsync(dbuf, h, n, cudaMemcpyHostToDevice, st);
+                    else if (kind == 1) e = launch_t1_copy(dh, dbuf, n / 16, n / 16, 0, 1, st);
+                    else e = cudaMemcpyAsync(h, dbuf, n, cudaMemcpyDeviceToHost, st);
+                }
+                if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+                if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+                float ms = 0.f;
+                if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+                if (e != cudaSuccess) {
+                    rc = TKV_ECUDA;
+                    break;
+                }
+                if (rep > 0 && ms > 0.f) best[kind] = std::max(best[kind], (double)n / (ms * 1e-3) / 1e9);
+            }
+        }
+    }
+    if (st) cudaStreamSynchronize(st);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    if (st) cudaStreamDestroy(st);
+    if (dbuf) cudaFree(dbuf);
+    if (h) cudaFreeHost(h);
+    (void)cudaGetLastError();
+    if (rc != TKV_OK) return rc;
+    if (h2d_ce_gbs) *h2d_ce_gbs = best[0];
+    if (h2d_sm_gbs) *h2d_sm_gbs = best[1];
+    if (d2h_ce_gbs) *d2h_ce_gbs = best[2];
+    return TKV_OK;
 }
 
 tkv_status tkv_get_stats(tkv_ctx* ctx, tkv_stats* out) {

@@ -53,7 +53,7 @@ struct RetierParams {
     int32_t pad[3];
 };
 
-__host__ __device__ inline uint32_t make_loc(int tier, int slot) {
+__host__ __device__ constexpr inline uint32_t make_loc(int tier, int slot) {
     return ((uint32_t)tier << 30) | (uint32_t)slot;
 }
 __host__ __device__ inline int loc_tier(uint32_t loc) { return (int)(loc >> 30); }

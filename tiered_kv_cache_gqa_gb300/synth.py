@@ -133,6 +133,11 @@ class Generator:
                                             torch.tensor(1.0, device=self.device))
         else:
             self.channel_gain = None
+        # Caches of values already drawn (pure memoisation: a value never depends on whether it
+        # came from a cache): heavy-hitter offsets per (sequence, block), and the last K/V block
+        # drawn per (sequence, layer), which successive decode positions share.
+        self._hh_cache = {}
+        self._blk_cache = {}
 
     # ----------------------------------------------------------- direction u
     def u_at(self, epoch: int):
@@ -172,20 +177,32 @@ class Generator:
     # ----------------------------------------------------------- K / V rows
     BLOCK = 64   # positions drawn together; a row's value does not depend on the slice asked for
 
+    def _hh_offsets(self, b: int, blk: int):
+        """Offsets within block `blk` of sequence b that are heavy hitters (a list)."""
+        key = (b, blk)
+        if key not in self._hh_cache:
+            hh = self.heavy_hitters(b, blk * self.BLOCK, self.BLOCK)
+            self._hh_cache[key] = torch.nonzero(hh).flatten().tolist()
+        return self._hh_cache[key]
+
     def _kv_block(self, b: int, layer: int, blk: int):
+        key = (b, layer)
+        hit = self._blk_cache.get(key)
+        if hit is not None and hit[0] == blk:
+            return hit[1]
         wl = self.wl
         Hkv, d, n = wl.num_kv_heads, wl.head_dim, self.BLOCK
         start = blk * n
         g = _gen(self.device, *_key(wl.seed, "kv", b, layer, blk))
         kv = torch.randn(2, Hkv, n, d, generator=g, device=self.device)
-        hh = self.heavy_hitters(b, start, n)
-        if bool(hh.any()):
-            for j in torch.nonzero(hh).flatten().tolist():
-                u = self.u_at(self.epoch_of_position(start + j))[layer]   # [Hkv, d]
-                kv[0, :, j, :] += wl.hh_gain * u
+        for j in self._hh_offsets(b, blk):
+            u = self.u_at(self.epoch_of_position(start + j))[layer]   # [Hkv, d]
+            kv[0, :, j, :] += wl.hh_gain * u
         if self.channel_gain is not None:
             kv = kv * self.channel_gain[:, layer][:, :, None, :]
-        return kv.to(torch.bfloat16)
+        kv = kv.to(torch.bfloat16)
+        self._blk_cache[key] = (blk, kv)
+        return kv
 
     def kv_rows(self, b: int, layer: int, start: int, n: int):
         """K, V of positions [start, start+n) of (sequence b, layer): [Hkv, n, d] bf16."""
