@@ -696,6 +696,8 @@ def main():
                               "note": "per-kernel events; roofline and transfer figures come from this pass"},
             "attention_step_ms": pa["ms"] / KP_,
             "host_link_measured": r["link"],
+            "host_stores": {"bytes": st["host_bytes_allocated"], "huge_page_bytes": st["host_huge_bytes"],
+                            "numa_node": st["host_numa_node"]},
             "t1_stream": dict(link_fraction(t1_gbs, r["link"]) or {}, bytes_per_step=p1["bytes"] / KP_,
                               ms_per_step=p1["ms"] / KP_, t2_bytes_total=st["h2d_bytes_t2_stream"],
                               note="host-link stream per layer: T1 rows, and T2 records with --t2 host"),

@@ -293,6 +293,36 @@ def test_t1_transports_are_bitwise_identical():
         assert np.array_equal(s, outs[0][1])
 
 
+def test_host_store_allocations_are_bitwise_identical():
+    """The large host stores as a huge-page arena registered with CUDA (default) or as
+    cudaHostAlloc blocks: the same bytes reach the kernel, so outputs, scores and tiers are
+    bit-identical across re-tiers that write back, quantise and promote through those stores."""
+    wl = synth.Workload("hostalloc", 2, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
+                        window=16, delta=32, ratios=(0.3, 0.5, 0.15, 0.05), seed=14)
+    runs = []
+    for mode in (tkv.TKV_HOST_HUGE_ARENA, tkv.TKV_HOST_PINNED_ALLOC):
+        for t2 in (tkv.TKV_T2_HBM, tkv.TKV_T2_HOST):
+            gen = synth.Generator(wl)
+            ctx = tkv.TieredKV.for_workload(wl, host_alloc=mode, t2_placement=t2)
+            prefill_both(ctx, None, gen)
+            out = torch.empty(wl.num_layers, wl.batch, wl.num_q_heads, wl.head_dim, device="cuda")
+            res = []
+            for t in range(1, 71):
+                q, k, v = gen.decode_step(t)
+                gpu_step(ctx, q.cuda(), k.cuda(), v.cuda(), out)
+                if t % wl.delta == 0:
+                    ctx.retier()
+                if t > 32:
+                    res.append(out.cpu().clone())
+            st = ctx.stats()
+            runs.append((torch.stack(res), ctx.scores(), ctx.tiers(), st))
+            ctx.close()
+    for o, s, t, st in runs[1:]:
+        assert torch.equal(o, runs[0][0])
+        assert np.array_equal(s, runs[0][1]) and np.array_equal(t, runs[0][2])
+    assert runs[2][3]["host_huge_bytes"] == 0 and runs[0][3]["host_huge_bytes"] >= 0
+
+
 def test_resident_t1_lockstep_with_the_oracle():
     """TKV_T1_RESIDENT (the HBM copy of T1 kept by the re-tier's moves) in lockstep with the
     fp64 oracle: out, s and tiers every step, across two re-tiers that demote, promote,

@@ -21,6 +21,7 @@ LIB_PATH = os.environ.get("TKV_LIBRARY") or os.path.join(_HERE, "libtkv.so")
 TKV_OK, TKV_EINVAL, TKV_ENOMEM, TKV_ECUDA, TKV_ECAPACITY, TKV_ETIMEOUT, TKV_ESTATE = range(7)
 TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY, TKV_T1_SPLIT, TKV_T1_MULTI_CE, TKV_T1_RESIDENT = range(5)
 TKV_T2_HBM, TKV_T2_HOST = range(2)
+TKV_HOST_HUGE_ARENA, TKV_HOST_PINNED_ALLOC = range(2)
 
 # Every function the C ABI exports (include/tkv.h).
 EXPORTS = ("tkv_create", "tkv_destroy", "tkv_append", "tkv_prefetch", "tkv_decode_step",
@@ -53,7 +54,7 @@ class Config(ctypes.Structure):
         ("t2_capacity", ctypes.c_int32), ("t1_transport", ctypes.c_int32),
         ("device", ctypes.c_int32),
         ("compute_stream", ctypes.c_void_p), ("copy_stream", ctypes.c_void_p),
-        ("t2_placement", ctypes.c_int32),
+        ("t2_placement", ctypes.c_int32), ("host_alloc", ctypes.c_int32),
     ]
 
 
@@ -69,7 +70,8 @@ class Stats(ctypes.Structure):
         ("hbm_bytes_kv_resident", ctypes.c_int64), ("kv_bytes_full_cache", ctypes.c_int64),
         ("kernel_launches", ctypes.c_int64),
         ("status", ctypes.c_int32), ("attn_splits", ctypes.c_int32),
-        ("h2d_bytes_t2_stream", ctypes.c_int64),
+        ("h2d_bytes_t2_stream", ctypes.c_int64), ("host_huge_bytes", ctypes.c_int64),
+        ("host_numa_node", ctypes.c_int32), ("pad0", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -276,7 +278,7 @@ class TieredKV:
                  prompt_len, num_sinks=4, recent_window=64, retier_interval=64,
                  ratios=(1.0, 0.0, 0.0, 0.0), t0_capacity=0, t1_capacity=0, t2_capacity=0,
                  t1_transport=TKV_T1_COPY_ENGINE, device=0, compute_stream=None, copy_stream=None,
-                 t2_placement=TKV_T2_HBM):
+                 t2_placement=TKV_T2_HBM, host_alloc=TKV_HOST_HUGE_ARENA):
         cfg = Config()
         cfg.num_layers, cfg.num_q_heads, cfg.num_kv_heads = num_layers, num_q_heads, num_kv_heads
         cfg.head_dim, cfg.batch, cfg.max_tokens = head_dim, batch, max_tokens
@@ -286,6 +288,7 @@ class TieredKV:
         cfg.t0_capacity, cfg.t1_capacity, cfg.t2_capacity = t0_capacity, t1_capacity, t2_capacity
         cfg.t1_transport = t1_transport
         cfg.t2_placement = t2_placement
+        cfg.host_alloc = host_alloc
         cfg.device = device
         if compute_stream is None:
             compute_stream = torch_stream_handle()

@@ -10,15 +10,29 @@
 // protected set follow "Four-tier classification".
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
 
+#include <sys/mman.h>
+#include <sys/syscall.h>
+#include <unistd.h>
+
 #include "../../include/tkv.h"
 #include "tkv_internal.cuh"
 
 using namespace tkv;
+
+// A large pinned host store (T1 rows, T2 masters, host T2 records): either a registered
+// anonymous mapping backed by transparent huge pages, or a cudaHostAlloc block.
+struct HostStore {
+    void* ptr = nullptr;      // what the library uses
+    void* map = nullptr;      // the mapping (huge-page arena), else null
+    size_t map_len = 0;
+    size_t huge_bytes = 0;    // bytes of the store backed by huge pages (from /proc/self/smaps)
+};
 
 struct tkv_ctx {
     tkv_config cfg{};
@@ -53,6 +67,8 @@ struct tkv_ctx {
     int32_t* pos_n = nullptr;                // [B] committed positions (device copy of N)
 
     // pinned host
+    HostStore hs_h1, hs_h2m, hs_t2;                   // the large stores
+    int host_numa = -1;                               // NUMA node the large stores are bound to, or -1
     __nv_bfloat16 *h1 = nullptr, *h2m = nullptr;      // host pointers
     __nv_bfloat16 *d_h1 = nullptr, *d_h2m = nullptr;  // device views
     RetierOut* h_outp = nullptr;
@@ -170,6 +186,134 @@ cudaError_t halloc(tkv_ctx* c, T** p, size_t n) {
     return e;
 }
 
+// ------------------------------------------------------------ host arenas
+// The T1 store of a large configuration is tens of GB of pinned host memory that the copy
+// engine reads once per decode step.  Backed by base pages (what cudaHostAlloc returns), its
+// translations can outgrow what the host link's DMA path keeps mapped, and the copy engine's
+// rate then drops well below the link's (measured on GB300 guests: 211 GB/s for a fresh
+// allocation falling to 15-110 GB/s once memory has been freed and reused).  Huge pages
+// keep the number of translations small.  So a large store is an anonymous mapping aligned
+// to the transparent-huge-page size, advised MADV_HUGEPAGE, bound to the host NUMA node
+// closest to the GPU when the host has several, populated, then registered with CUDA
+// (mapped, portable).  If any step of that fails, the store falls back to cudaHostAlloc.
+
+size_t thp_size() {
+    size_t v = 0;
+    if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+        unsigned long long x = 0;
+        if (std::fscanf(f, "%llu", &x) == 1) v = (size_t)x;
+        std::fclose(f);
+    }
+    return v >= 4096 && (v & (v - 1)) == 0 ? v : (size_t)2 << 20;
+}
+
+// Online NUMA nodes of the host (1 when unknown).
+int online_nodes() {
+    int n = 1;
+    if (FILE* f = std::fopen("/sys/devices/system/node/online", "r")) {
+        char buf[256] = {0};
+        if (std::fgets(buf, sizeof(buf), f)) {
+            // "0", "0-1", "0,2-3": count the ids
+            n = 0;
+            const char* p = buf;
+            while (*p) {
+                char* e = nullptr;
+                const long a = std::strtol(p, &e, 10);
+                if (e == p) break;
+                long b = a;
+                p = e;
+                if (*p == '-') {
+                    b = std::strtol(p + 1, &e, 10);
+                    p = e;
+                }
+                n += (int)(b - a + 1);
+                if (*p == ',') ++p;
+                else break;
+            }
+            if (n < 1) n = 1;
+        }
+        std::fclose(f);
+    }
+    return n;
+}
+
+// AnonHugePages of the mapping that contains `addr`, in bytes (0 when unknown).
+size_t huge_bytes_of(const void* addr) {
+    FILE* f = std::fopen("/proc/self/smaps", "r");
+    if (!f) return 0;
+    char line[512];
+    bool in = false;
+    size_t out = 0;
+    const unsigned long long a = (unsigned long long)(uintptr_t)addr;
+    while (std::fgets(line, sizeof(line), f)) {
+        unsigned long long lo = 0, hi = 0;
+        if (std::sscanf(line, "%llx-%llx ", &lo, &hi) == 2 && std::strchr(line, '-') < std::strchr(line, ' ')) {
+            in = a >= lo && a < hi;
+            continue;
+        }
+        unsigned long long kb = 0;
+        if (in && std::sscanf(line, "AnonHugePages: %llu kB", &kb) == 1) {
+            out = (size_t)kb * 1024;
+            break;
+        }
+    }
+    std::fclose(f);
+    return out;
+}
+
+cudaError_t harena_alloc(tkv_ctx* c, HostStore& hs, size_t bytes) {
+    hs = HostStore();
+    if (bytes == 0) return cudaSuccess;
+    if (c->cfg.host_alloc != TKV_HOST_PINNED_ALLOC) {
+        const size_t huge = thp_size();
+        const size_t body = (bytes + huge - 1) / huge * huge;
+        const size_t len = body + huge;
+        void* m = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+        if (m != MAP_FAILED) {
+            char* p = (char*)(((uintptr_t)m + huge - 1) / huge * huge);
+            if (c->host_numa >= 0) {
+                unsigned long mask[16] = {0};
+                if (c->host_numa < 1024) {
+                    mask[c->host_numa / 64] = 1ul << (c->host_numa % 64);
+                    // MPOL_BIND = 2; a refusal leaves the default policy
+                    if (syscall(SYS_mbind, p, body, 2, mask, 1024ul, 0u) != 0) c->host_numa = -1;
+                }
+            }
+            madvise(p, body, MADV_HUGEPAGE);
+            // populate (MADV_POPULATE_WRITE = 23), else touch every page
+            if (madvise(p, body, 23) != 0) {
+                const long pg = sysconf(_SC_PAGESIZE) > 0 ? sysconf(_SC_PAGESIZE) : 4096;
+                for (size_t o = 0; o < body; o += (size_t)pg) ((volatile char*)p)[o] = 0;
+            }
+            if (cudaHostRegister(p, body, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+                hs.ptr = p;
+                hs.map = m;
+                hs.map_len = len;
+                hs.huge_bytes = std::min(huge_bytes_of(p), body);
+                c->host_alloc += body;
+                return cudaSuccess;
+            }
+            (void)cudaGetLastError();
+            munmap(m, len);
+        }
+    }
+    cudaError_t e = cudaHostAlloc(&hs.ptr, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e == cudaSuccess) c->host_alloc += bytes;
+    else hs.ptr = nullptr;
+    return e;
+}
+
+void harena_free(HostStore& hs) {
+    if (!hs.ptr) return;
+    if (hs.map) {
+        cudaHostUnregister(hs.ptr);
+        munmap(hs.map, hs.map_len);
+    } else {
+        cudaFreeHost(hs.ptr);
+    }
+    hs = HostStore();
+}
+
 int protected_count(int N, int prompt, int sinks, int W) {
     const int a = std::min(N, std::max(prompt, sinks));
     const int w0 = std::max(0, N - W);
@@ -180,7 +324,7 @@ size_t row_bytes_bf16(const tkv_ctx* c) { return (size_t)2 * c->Hkv * c->d * 2; 
 
 void free_all(tkv_ctx* c) {
     cudaFree(c->k0v0); cudaFree(c->stage); cudaFree(c->stage2);
-    if (c->t2_host) cudaFreeHost(c->t2_host);
+    if (c->t2_host) harena_free(c->hs_t2);
     else cudaFree(c->t2);
     cudaFree(c->tier); cudaFree(c->new_tier); cudaFree(c->forced);
     cudaFree(c->slot); cudaFree(c->new_slot); cudaFree(c->free_scratch);
@@ -188,7 +332,7 @@ void free_all(tkv_ctx* c) {
     cudaFree(c->g); cudaFree(c->part); cudaFree(c->zs); cudaFree(c->t0_free); cudaFree(c->t0_top);
     cudaFree(c->moves_now); cudaFree(c->moves_delta); cudaFree(c->outp); cudaFree(c->params);
     cudaFree(c->err); cudaFree(c->pos_n);
-    cudaFreeHost(c->h1); cudaFreeHost(c->h2m); cudaFreeHost(c->h_outp); cudaFreeHost(c->h_params);
+    harena_free(c->hs_h1); harena_free(c->hs_h2m); cudaFreeHost(c->h_outp); cudaFreeHost(c->h_params);
     cudaFreeHost(c->h_err);
     for (int i = 0; i < 2; ++i) {
         if (c->ev_t1[i]) cudaEventDestroy(c->ev_t1[i]);
@@ -528,6 +672,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     if (c.t0_capacity < 0 || c.t1_capacity < 0 || c.t2_capacity < 0) return TKV_EINVAL;
     if (c.t1_transport < TKV_T1_COPY_ENGINE || c.t1_transport > TKV_T1_RESIDENT) return TKV_EINVAL;
     if (c.t2_placement != TKV_T2_HBM && c.t2_placement != TKV_T2_HOST) return TKV_EINVAL;
+    if (c.host_alloc != TKV_HOST_HUGE_ARENA && c.host_alloc != TKV_HOST_PINNED_ALLOC) return TKV_EINVAL;
     const float r[4] = {c.ratio_t0, c.ratio_t1, c.ratio_t2, c.ratio_t3};
     int64_t ppm[4], sum = 0;
     for (int i = 0; i < 4; ++i) {
@@ -608,9 +753,18 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
         (void)cudaGetLastError();
         return bail(TKV_ENOMEM);
     }
-    A(halloc(ctx, &ctx->h1, L * 2 * B * Hkv * S1 * d));
-    A(halloc(ctx, &ctx->h2m, L * 2 * B * Hkv * S2 * d));
-    if (t2_host) A(halloc(ctx, &ctx->t2_host, L * 2 * B * Hkv * S2 * (d + 16)));
+    {
+        int numa = -1;
+        if (online_nodes() > 1 && cudaDeviceGetAttribute(&numa, cudaDevAttrHostNumaId, c.device) == cudaSuccess)
+            ctx->host_numa = numa;
+        (void)cudaGetLastError();
+    }
+    A(harena_alloc(ctx, ctx->hs_h1, L * 2 * B * Hkv * S1 * d * sizeof(__nv_bfloat16)));
+    A(harena_alloc(ctx, ctx->hs_h2m, L * 2 * B * Hkv * S2 * d * sizeof(__nv_bfloat16)));
+    if (t2_host) A(harena_alloc(ctx, ctx->hs_t2, L * 2 * B * Hkv * S2 * (d + 16)));
+    ctx->h1 = (__nv_bfloat16*)ctx->hs_h1.ptr;
+    ctx->h2m = (__nv_bfloat16*)ctx->hs_h2m.ptr;
+    ctx->t2_host = (uint8_t*)ctx->hs_t2.ptr;
     A(halloc(ctx, &ctx->h_outp, B));
     A(halloc(ctx, &ctx->h_params, B));
     A(halloc(ctx, &ctx->h_err, 1));
@@ -1181,6 +1335,8 @@ tkv_status tkv_get_stats(tkv_ctx* ctx, tkv_stats* out) {
     s.kernel_launches = ctx->launches;
     s.status = ctx->status;
     s.attn_splits = ctx->last_splits;
+    s.host_huge_bytes = (int64_t)(ctx->hs_h1.huge_bytes + ctx->hs_h2m.huge_bytes + ctx->hs_t2.huge_bytes);
+    s.host_numa_node = ctx->host_numa;
     *out = s;
     return TKV_OK;
 }
