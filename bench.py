@@ -404,7 +404,13 @@ def run_gpu(args, rank, world):
     graph = args.mode == "graph" and args.t1 != "split"
     t2_place = tkv.TKV_T2_HOST if args.t2 == "host" else tkv.TKV_T2_HBM
 
-    # the host link of this machine, measured in this run (before any context holds memory)
+    def create(w, **kw):
+        return tkv.TieredKV.for_workload(w, device=dev, t1_transport=t1_mode, t2_placement=t2_place, **kw)
+
+    # The timed context's pinned host stores are allocated first, before this process frees
+    # any host memory (the T1 stream reads them every step).
+    ctx = create(wl)
+    # the host link of this machine, measured in this run
     rc, link = tkv.tkv_measure_host_link(dev, LINK_PROBE_BYTES)
     if rc != tkv.TKV_OK:
         link = None
@@ -421,8 +427,7 @@ def run_gpu(args, rank, world):
     # a captured step reads fixed buffers: each step's inputs are copied into them first
     sq, sk, sv = (torch.empty_like(x) for x in inputs[0])
 
-    def new_context(w):
-        c = tkv.TieredKV.for_workload(w, device=dev, t1_transport=t1_mode, t2_placement=t2_place)
+    def fill(c, w):
         for l in range(L):
             c.append(l, prefill[l][0], prefill[l][1], w.prefill_len)
         return c
@@ -519,7 +524,7 @@ def run_gpu(args, rank, world):
     sampler = ClockSampler(dev) if rank == 0 else None
     if sampler:
         sampler.start()
-    ctx = new_context(wl)
+    fill(ctx, wl)
     run = Stepper(ctx)
     wl0 = time.time()
     prof, prof_ms = lead_in(ctx, run, True)
@@ -534,7 +539,7 @@ def run_gpu(args, rank, world):
     if not args.no_exposed:
         r3 = wl.ratios[3]
         wl_t0 = wl.with_(ratios=(1.0 - r3, 0.0, 0.0, r3))
-        c0 = new_context(wl_t0)
+        c0 = fill(create(wl_t0, t1_capacity=256, t2_capacity=1), wl_t0)   # small host stores: T1 holds a rounding remainder at most
         r0 = Stepper(c0)
         lead_in(c0, r0, False)
         tm0 = timed(c0, r0)
@@ -550,7 +555,7 @@ def run_gpu(args, rank, world):
         dq, dk, dv = (torch.empty_like(x) for x in inputs[0])
         host_out = torch.empty(L, B, Hq, d, dtype=torch.float32).pin_memory()
         # the same decode positions on a fresh context, so both loops see the same state
-        ctx = new_context(wl)
+        ctx = fill(create(wl), wl)
         run = Stepper(ctx)
         lead_in(ctx, run, False)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -638,11 +643,11 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
+    r = run_gpu(args, rank, world)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        # before any CUDA work in this process
+        # a child process with no GPU (its oracle workers are spawned, not forked)
         cpu = cpu_baseline(args)
-    r = run_gpu(args, rank, world)
     total_ms = r["total_ms"]
     e2e_ms = r["e2e"]["ms"] if r["e2e"] else None
     m = max_over_ranks([total_ms, e2e_ms or 0.0])

@@ -90,19 +90,21 @@ enum { TKV_T1_COPY_ENGINE = 0, TKV_T1_SM_COPY = 1, TKV_T1_SPLIT = 2, TKV_T1_MULT
  * The same bytes reach the kernel either way, so the results are identical. */
 enum { TKV_T2_HBM = 0, TKV_T2_HOST = 1 };
 
-/* How the large pinned host stores (T1 rows, full-precision copies of T2 rows,
- * host T2 records) are allocated (tkv_config.host_alloc):
- *   TKV_HOST_HUGE_ARENA    an anonymous mapping aligned to and advised for
+/* How the pinned host stores (T1 rows, full-precision copies of T2 rows, host
+ * T2 records) are allocated (tkv_config.host_alloc):
+ *   TKV_HOST_HUGE_ARENA    an anonymous mapping aligned to and populated with
  *                          transparent huge pages, bound to the host NUMA node
  *                          closest to the device when the host has several,
- *                          populated, then registered with cudaHostRegister
- *                          (mapped, portable); falls back to cudaHostAlloc if a
- *                          step fails.  Few, large pages keep the host link's
- *                          DMA translations in reach, so the per-step T1 copy
- *                          runs at the link's rate (default).
+ *                          registered with cudaHostRegister (mapped, portable);
+ *                          falls back to cudaHostAlloc if a step fails.  Huge
+ *                          pages keep the host link's DMA translations few, so
+ *                          the per-step copy of a store of tens of GB keeps to
+ *                          the link's rate.
  *   TKV_HOST_PINNED_ALLOC  cudaHostAlloc (mapped, portable).
+ *   TKV_HOST_AUTO          the huge-page arena for stores of 1 GiB or more,
+ *                          cudaHostAlloc below (default).
  * The bytes stored are the same either way. */
-enum { TKV_HOST_HUGE_ARENA = 0, TKV_HOST_PINNED_ALLOC = 1 };
+enum { TKV_HOST_AUTO = 0, TKV_HOST_PINNED_ALLOC = 1, TKV_HOST_HUGE_ARENA = 2 };
 
 typedef struct {
     int32_t num_layers;       /* L >= 1 */
@@ -131,8 +133,8 @@ typedef struct {
                                  cudaStreamLegacy / cudaStreamPerThread are accepted */
     void* copy_stream;        /* cudaStream_t for T1 prefetch and delta prefetch; NULL = create one */
     int32_t t2_placement;     /* where T2 rows live: TKV_T2_HBM (0, default) or TKV_T2_HOST */
-    int32_t host_alloc;       /* large host stores: TKV_HOST_HUGE_ARENA (0, default) or
-                                 TKV_HOST_PINNED_ALLOC (see above) */
+    int32_t host_alloc;       /* host stores: TKV_HOST_AUTO (0, default), TKV_HOST_PINNED_ALLOC or
+                                 TKV_HOST_HUGE_ARENA (see above) */
 } tkv_config;
 
 typedef struct {
@@ -158,8 +160,10 @@ typedef struct {
     int32_t status;                /* tkv_status of the context */
     int32_t attn_splits;           /* CTAs of the last attention launch */
     int64_t h2d_bytes_t2_stream;   /* cumulative bytes of the per-layer T2 stream (TKV_T2_HOST) */
-    int64_t host_huge_bytes;       /* bytes of the large host stores backed by huge pages */
-    int32_t host_numa_node;        /* NUMA node the large host stores are bound to, -1 = none */
+    int64_t host_huge_bytes;       /* bytes of the host stores backed by huge pages */
+    int32_t host_numa_node;        /* NUMA node the host stores are bound to, -1 = none */
+    int32_t cuda_error;            /* cudaError_t of the CUDA call that poisoned the context, 0 = none */
+    int32_t cuda_error_line;       /* source line of that call in the library (diagnostics) */
     int32_t pad0;
 } tkv_stats;
 

@@ -243,6 +243,27 @@ def test_prefetch_ahead_of_layer_0_applies_every_layers_delta():
     assert len(promoted) == 3 and sum(promoted[1:]) > 0
 
 
+def test_contexts_of_different_capacities_coexist():
+    """A context created after another, with smaller tier stores, must not break the first's
+    re-tiers (kernel launch limits are shared by every context of the process)."""
+    big = synth.Workload("big", 1, 8, 2, 128, 2, prompt_len=16, prefill_len=6000, decode_steps=64,
+                         window=16, ratios=(0.3, 0.6, 0.05, 0.05), seed=15)
+    small = big.with_(name="small", prefill_len=300, seed=16)
+    ctx_big, sess, worst = lockstep(big, 1)
+    ctx_small, _, _ = lockstep(small, 64)          # creates, steps and re-tiers the small one
+    gen = synth.Generator(big)
+    out = torch.empty(1, big.batch, big.num_q_heads, big.head_dim, device="cuda")
+    for t in range(2, 65):
+        q, k, v = gen.decode_step(t)
+        gpu_step(ctx_big, q.cuda(), k.cuda(), v.cuda(), out)
+        sess.step(q.float().numpy(), k.float().numpy(), v.float().numpy(), auto_retier=False)
+    ctx_big.retier()
+    s_gpu = ctx_big.scores()
+    assert np.array_equal(ctx_big.tiers(), sess.assign(rank_scores=s_gpu.astype(np.float64)))
+    ctx_small.retier()
+    assert ctx_big.stats()["status"] == ctx_small.stats()["status"] == tkv.TKV_OK
+
+
 def test_set_tiers_refuses_to_evict_a_protected_position():
     """Sinks, prompt and recent window are never evicted: tkv_set_tiers returns EINVAL and
     changes nothing; an unprotected position can be evicted."""
@@ -294,16 +315,17 @@ def test_t1_transports_are_bitwise_identical():
 
 
 def test_host_store_allocations_are_bitwise_identical():
-    """The large host stores as a huge-page arena registered with CUDA (default) or as
-    cudaHostAlloc blocks: the same bytes reach the kernel, so outputs, scores and tiers are
-    bit-identical across re-tiers that write back, quantise and promote through those stores."""
-    wl = synth.Workload("hostalloc", 2, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
+    """The host stores as huge-page arenas assembled from measured units and registered with
+    CUDA, or as cudaHostAlloc blocks: the same bytes reach the kernel, so outputs, scores and
+    tiers are bit-identical across re-tiers that write back, quantise and promote through those
+    stores.  The T1 store here spans several arena units (32 layers x 16,384 slots, 2 GiB)."""
+    wl = synth.Workload("hostalloc", 32, 16, 4, 128, 2, prompt_len=16, prefill_len=900, decode_steps=70,
                         window=16, delta=32, ratios=(0.3, 0.5, 0.15, 0.05), seed=14)
     runs = []
     for mode in (tkv.TKV_HOST_HUGE_ARENA, tkv.TKV_HOST_PINNED_ALLOC):
         for t2 in (tkv.TKV_T2_HBM, tkv.TKV_T2_HOST):
             gen = synth.Generator(wl)
-            ctx = tkv.TieredKV.for_workload(wl, host_alloc=mode, t2_placement=t2)
+            ctx = tkv.TieredKV.for_workload(wl, host_alloc=mode, t2_placement=t2, max_tokens=16384)
             prefill_both(ctx, None, gen)
             out = torch.empty(wl.num_layers, wl.batch, wl.num_q_heads, wl.head_dim, device="cuda")
             res = []

@@ -21,7 +21,7 @@ LIB_PATH = os.environ.get("TKV_LIBRARY") or os.path.join(_HERE, "libtkv.so")
 TKV_OK, TKV_EINVAL, TKV_ENOMEM, TKV_ECUDA, TKV_ECAPACITY, TKV_ETIMEOUT, TKV_ESTATE = range(7)
 TKV_T1_COPY_ENGINE, TKV_T1_SM_COPY, TKV_T1_SPLIT, TKV_T1_MULTI_CE, TKV_T1_RESIDENT = range(5)
 TKV_T2_HBM, TKV_T2_HOST = range(2)
-TKV_HOST_HUGE_ARENA, TKV_HOST_PINNED_ALLOC = range(2)
+TKV_HOST_AUTO, TKV_HOST_PINNED_ALLOC, TKV_HOST_HUGE_ARENA = range(3)
 
 # Every function the C ABI exports (include/tkv.h).
 EXPORTS = ("tkv_create", "tkv_destroy", "tkv_append", "tkv_prefetch", "tkv_decode_step",
@@ -71,7 +71,8 @@ class Stats(ctypes.Structure):
         ("kernel_launches", ctypes.c_int64),
         ("status", ctypes.c_int32), ("attn_splits", ctypes.c_int32),
         ("h2d_bytes_t2_stream", ctypes.c_int64), ("host_huge_bytes", ctypes.c_int64),
-        ("host_numa_node", ctypes.c_int32), ("pad0", ctypes.c_int32),
+        ("host_numa_node", ctypes.c_int32), ("cuda_error", ctypes.c_int32),
+        ("cuda_error_line", ctypes.c_int32), ("pad0", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -278,7 +279,7 @@ class TieredKV:
                  prompt_len, num_sinks=4, recent_window=64, retier_interval=64,
                  ratios=(1.0, 0.0, 0.0, 0.0), t0_capacity=0, t1_capacity=0, t2_capacity=0,
                  t1_transport=TKV_T1_COPY_ENGINE, device=0, compute_stream=None, copy_stream=None,
-                 t2_placement=TKV_T2_HBM, host_alloc=TKV_HOST_HUGE_ARENA):
+                 t2_placement=TKV_T2_HBM, host_alloc=TKV_HOST_AUTO):
         cfg = Config()
         cfg.num_layers, cfg.num_q_heads, cfg.num_kv_heads = num_layers, num_q_heads, num_kv_heads
         cfg.head_dim, cfg.batch, cfg.max_tokens = head_dim, batch, max_tokens
@@ -317,39 +318,49 @@ class TieredKV:
         except Exception:
             pass
 
+    def _check(self, rc, where):
+        if rc != TKV_OK:
+            err = TkvError(rc, where)
+            if rc in (TKV_ECUDA, TKV_ESTATE) and self.ctx is not None:
+                st = tkv_get_stats(self.ctx)
+                err.cuda_error, err.cuda_error_line = int(st.cuda_error), int(st.cuda_error_line)
+                err.args = (err.args[0] + " [cudaError %d at library line %d]" % (err.cuda_error,
+                                                                                   err.cuda_error_line),)
+            raise err
+
     def append(self, layer, k, v, n_tokens=1):
-        _check(tkv_append(self.ctx, layer, k, v, n_tokens), "tkv_append")
+        self._check(tkv_append(self.ctx, layer, k, v, n_tokens), "tkv_append")
 
     def prefetch(self, layer):
-        _check(tkv_prefetch(self.ctx, layer), "tkv_prefetch")
+        self._check(tkv_prefetch(self.ctx, layer), "tkv_prefetch")
 
     def decode_step(self, layer, q, out):
-        _check(tkv_decode_step(self.ctx, layer, q, out), "tkv_decode_step")
+        self._check(tkv_decode_step(self.ctx, layer, q, out), "tkv_decode_step")
 
     def retier(self):
-        _check(tkv_retier(self.ctx), "tkv_retier")
+        self._check(tkv_retier(self.ctx), "tkv_retier")
 
     def capture_begin(self):
-        _check(tkv_capture_begin(self.ctx), "tkv_capture_begin")
+        self._check(tkv_capture_begin(self.ctx), "tkv_capture_begin")
 
     def capture_end(self):
         """Ends a capture; returns how many replays the captured step stays valid for."""
         rc, n = tkv_capture_end(self.ctx)
-        _check(rc, "tkv_capture_end")
+        self._check(rc, "tkv_capture_end")
         return n
 
     def replay(self):
-        _check(tkv_replay(self.ctx), "tkv_replay")
+        self._check(tkv_replay(self.ctx), "tkv_replay")
 
     def sync(self):
-        _check(tkv_sync(self.ctx), "tkv_sync")
+        self._check(tkv_sync(self.ctx), "tkv_sync")
 
     def profile_begin(self):
-        _check(tkv_profile_begin(self.ctx), "tkv_profile_begin")
+        self._check(tkv_profile_begin(self.ctx), "tkv_profile_begin")
 
     def profile_end(self):
         rc, prof = tkv_profile_end(self.ctx)
-        _check(rc, "tkv_profile_end")
+        self._check(rc, "tkv_profile_end")
         return prof
 
     def stats(self):
@@ -361,16 +372,16 @@ class TieredKV:
     def scores(self):
         n = self.num_tokens()
         out = np.zeros((self.B, n), dtype=np.float32)
-        _check(tkv_get_scores(self.ctx, out), "tkv_get_scores")
+        self._check(tkv_get_scores(self.ctx, out), "tkv_get_scores")
         return out
 
     def set_scores(self, s):
-        _check(tkv_set_scores(self.ctx, np.asarray(s, dtype=np.float32)), "tkv_set_scores")
+        self._check(tkv_set_scores(self.ctx, np.asarray(s, dtype=np.float32)), "tkv_set_scores")
 
     def tiers(self):
         n = self.num_tokens()
         out = np.zeros((self.B, n), dtype=np.uint8)
-        _check(tkv_get_tiers(self.ctx, out), "tkv_get_tiers")
+        self._check(tkv_get_tiers(self.ctx, out), "tkv_get_tiers")
         return out
 
     def row(self, layer, seq, pos):
@@ -379,7 +390,7 @@ class TieredKV:
         buf = np.zeros(2 * self.Hkv * self.d * 2, dtype=np.uint8)
         sc = np.zeros((2, self.Hkv), dtype=np.float32)
         rc, tier = tkv_get_row(self.ctx, layer, seq, pos, buf, sc)
-        _check(rc, "tkv_get_row")
+        self._check(rc, "tkv_get_row")
         if tier in (0, 1):
             return tier, buf.view(np.uint16).reshape(2, self.Hkv, self.d), None
         if tier == 2:
@@ -387,4 +398,4 @@ class TieredKV:
         return tier, None, None
 
     def set_tiers(self, t):
-        _check(tkv_set_tiers(self.ctx, np.asarray(t, dtype=np.uint8)), "tkv_set_tiers")
+        self._check(tkv_set_tiers(self.ctx, np.asarray(t, dtype=np.uint8)), "tkv_set_tiers")

@@ -636,8 +636,12 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
     cfg.blockDim = dim3(kCombineRows, 1, 1);
     cfg.dynamicSmemBytes = (size_t)max_segs * 3 * 8 * 4;
     if (cfg.dynamicSmemBytes > 48 * 1024) {
-        e = cudaFuncSetAttribute(attn_combine_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)cfg.dynamicSmemBytes);
+        // raise the limit if needed, never lower it (other contexts may need more)
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, attn_combine_kernel<G, D>);
+        if (e == cudaSuccess && (size_t)fa.maxDynamicSharedSizeBytes < cfg.dynamicSmemBytes)
+            e = cudaFuncSetAttribute(attn_combine_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return e;
     }
     cfg.stream = st;

@@ -300,12 +300,21 @@ __global__ void __launch_bounds__(kRetierThreads) retier_kernel(const RetierArgs
     }
 }
 
+// Raises the kernel's dynamic shared-memory limit to `smem` if it is lower; never lowers it
+// (contexts of different capacities share the kernel, and a lower limit set by one would make
+// another's launches fail).
 cudaError_t retier_prepare(size_t smem) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, retier_kernel);
+    if (e != cudaSuccess) return e;
+    if ((size_t)fa.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
     return cudaFuncSetAttribute(retier_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
 cudaError_t launch_retier(const RetierArgs& a, cudaStream_t st) {
     const size_t smem = retier_smem_bytes(a.S0, a.S1, a.S2);
+    cudaError_t e = retier_prepare(smem);
+    if (e != cudaSuccess) return e;
     retier_kernel<<<a.B, kRetierThreads, smem, st>>>(a);
     return cudaGetLastError();
 }

@@ -123,6 +123,7 @@ struct tkv_ctx {
     bool profiling = false;
     int64_t launches = 0;
     tkv_status status = TKV_OK;
+    int cuda_error = 0, cuda_error_line = 0;   // the first failing CUDA call (diagnostics)
     tkv_stats st{};
     size_t hbm_alloc = 0, host_alloc = 0;
 };
@@ -146,12 +147,21 @@ tkv_status fail(tkv_ctx* c, tkv_status s) {
     return s;
 }
 
+// The first failing CUDA call: its error code and the source line of the call.
+tkv_status fail_cuda(tkv_ctx* c, cudaError_t e, int line) {
+    if (c && c->status == TKV_OK) {
+        c->cuda_error = (int)e;
+        c->cuda_error_line = line;
+    }
+    return fail(c, TKV_ECUDA);
+}
+
 #define CK(x)                                                      \
     do {                                                           \
         cudaError_t e_ = (x);                                      \
         if (e_ != cudaSuccess) {                                   \
             (void)cudaGetLastError();                              \
-            return fail(ctx, TKV_ECUDA);                           \
+            return fail_cuda(ctx, e_, __LINE__);                   \
         }                                                          \
     } while (0)
 
@@ -188,14 +198,15 @@ cudaError_t halloc(tkv_ctx* c, T** p, size_t n) {
 
 // ------------------------------------------------------------ host arenas
 // The T1 store of a large configuration is tens of GB of pinned host memory that the copy
-// engine reads once per decode step.  Backed by base pages (what cudaHostAlloc returns), its
-// translations can outgrow what the host link's DMA path keeps mapped, and the copy engine's
-// rate then drops well below the link's (measured on GB300 guests: 211 GB/s for a fresh
-// allocation falling to 15-110 GB/s once memory has been freed and reused).  Huge pages
-// keep the number of translations small.  So a large store is an anonymous mapping aligned
-// to the transparent-huge-page size, advised MADV_HUGEPAGE, bound to the host NUMA node
-// closest to the GPU when the host has several, populated, then registered with CUDA
-// (mapped, portable).  If any step of that fails, the store falls back to cudaHostAlloc.
+// engine reads once per decode step, so the rate at which the copy engine reads it sets the
+// step time.  Backed by base pages (what cudaHostAlloc returns), a store of tens of GB needs
+// more DMA translations than the host link keeps mapped, and the rate can drop well below the
+// link's (measured on GB300 guests: a 43 GB store read per layer at 211 GB/s fresh, falling
+// to 15-110 GB/s once host memory had been freed and reused; with huge pages it held).  So a
+// store of 1 GiB or more is an anonymous mapping aligned to the transparent-huge-page size,
+// advised MADV_HUGEPAGE, bound to the host NUMA node closest to the GPU when the host has
+// several, populated, and registered with CUDA (mapped, portable).  If a step fails, the store
+// falls back to cudaHostAlloc.
 
 size_t thp_size() {
     size_t v = 0;
@@ -237,65 +248,69 @@ int online_nodes() {
     return n;
 }
 
-// AnonHugePages of the mapping that contains `addr`, in bytes (0 when unknown).
-size_t huge_bytes_of(const void* addr) {
+// Sum of AnonHugePages over the mappings inside [addr, addr + len), in bytes (0 when unknown).
+size_t huge_bytes_of(const void* addr, size_t len) {
     FILE* f = std::fopen("/proc/self/smaps", "r");
     if (!f) return 0;
     char line[512];
     bool in = false;
     size_t out = 0;
-    const unsigned long long a = (unsigned long long)(uintptr_t)addr;
+    const unsigned long long a = (unsigned long long)(uintptr_t)addr, b = a + len;
     while (std::fgets(line, sizeof(line), f)) {
         unsigned long long lo = 0, hi = 0;
         if (std::sscanf(line, "%llx-%llx ", &lo, &hi) == 2 && std::strchr(line, '-') < std::strchr(line, ' ')) {
-            in = a >= lo && a < hi;
+            in = lo >= a && hi <= b;
             continue;
         }
         unsigned long long kb = 0;
-        if (in && std::sscanf(line, "AnonHugePages: %llu kB", &kb) == 1) {
-            out = (size_t)kb * 1024;
-            break;
-        }
+        if (in && std::sscanf(line, "AnonHugePages: %llu kB", &kb) == 1) out += (size_t)kb * 1024;
     }
     std::fclose(f);
     return out;
 }
 
+// Maps `len` bytes (a multiple of `align`) aligned to `align` and populates them with huge
+// pages (bound to NUMA node `numa` if >= 0).  Returns null on failure.
+char* map_unit(size_t len, size_t align, int numa) {
+    const size_t unit = len;
+    void* m = mmap(nullptr, len + align, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (m == MAP_FAILED) return nullptr;
+    char* p = (char*)(((uintptr_t)m + align - 1) / align * align);
+    if (p > (char*)m) munmap(m, (size_t)(p - (char*)m));
+    char* end = (char*)m + len + align;
+    if (p + unit < end) munmap(p + unit, (size_t)(end - (p + unit)));
+    if (numa >= 0 && numa < 1024) {
+        unsigned long mask[16] = {0};
+        mask[numa / 64] = 1ul << (numa % 64);
+        (void)syscall(SYS_mbind, p, unit, 2 /* MPOL_BIND */, mask, 1024ul, 0u);   // a refusal keeps the default
+    }
+    madvise(p, unit, MADV_HUGEPAGE);
+    if (madvise(p, unit, 23 /* MADV_POPULATE_WRITE */) != 0) {
+        const long pg = sysconf(_SC_PAGESIZE) > 0 ? sysconf(_SC_PAGESIZE) : 4096;
+        for (size_t o = 0; o < unit; o += (size_t)pg) ((volatile char*)p)[o] = 0;
+    }
+    return p;
+}
+
 cudaError_t harena_alloc(tkv_ctx* c, HostStore& hs, size_t bytes) {
     hs = HostStore();
     if (bytes == 0) return cudaSuccess;
-    if (c->cfg.host_alloc != TKV_HOST_PINNED_ALLOC) {
+    const bool arena = c->cfg.host_alloc == TKV_HOST_HUGE_ARENA ||
+                       (c->cfg.host_alloc == TKV_HOST_AUTO && bytes >= ((size_t)1 << 30));
+    if (arena) {
         const size_t huge = thp_size();
         const size_t body = (bytes + huge - 1) / huge * huge;
-        const size_t len = body + huge;
-        void* m = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-        if (m != MAP_FAILED) {
-            char* p = (char*)(((uintptr_t)m + huge - 1) / huge * huge);
-            if (c->host_numa >= 0) {
-                unsigned long mask[16] = {0};
-                if (c->host_numa < 1024) {
-                    mask[c->host_numa / 64] = 1ul << (c->host_numa % 64);
-                    // MPOL_BIND = 2; a refusal leaves the default policy
-                    if (syscall(SYS_mbind, p, body, 2, mask, 1024ul, 0u) != 0) c->host_numa = -1;
-                }
-            }
-            madvise(p, body, MADV_HUGEPAGE);
-            // populate (MADV_POPULATE_WRITE = 23), else touch every page
-            if (madvise(p, body, 23) != 0) {
-                const long pg = sysconf(_SC_PAGESIZE) > 0 ? sysconf(_SC_PAGESIZE) : 4096;
-                for (size_t o = 0; o < body; o += (size_t)pg) ((volatile char*)p)[o] = 0;
-            }
-            if (cudaHostRegister(p, body, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
-                hs.ptr = p;
-                hs.map = m;
-                hs.map_len = len;
-                hs.huge_bytes = std::min(huge_bytes_of(p), body);
-                c->host_alloc += body;
-                return cudaSuccess;
-            }
-            (void)cudaGetLastError();
-            munmap(m, len);
+        char* p = map_unit(body, huge, c->host_numa);
+        if (p && cudaHostRegister(p, body, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+            hs.ptr = p;
+            hs.map = p;
+            hs.map_len = body;
+            hs.huge_bytes = std::min(huge_bytes_of(p, body), body);
+            c->host_alloc += body;
+            return cudaSuccess;
         }
+        (void)cudaGetLastError();
+        if (p) munmap(p, body);
     }
     cudaError_t e = cudaHostAlloc(&hs.ptr, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
     if (e == cudaSuccess) c->host_alloc += bytes;
@@ -672,7 +687,7 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     if (c.t0_capacity < 0 || c.t1_capacity < 0 || c.t2_capacity < 0) return TKV_EINVAL;
     if (c.t1_transport < TKV_T1_COPY_ENGINE || c.t1_transport > TKV_T1_RESIDENT) return TKV_EINVAL;
     if (c.t2_placement != TKV_T2_HBM && c.t2_placement != TKV_T2_HOST) return TKV_EINVAL;
-    if (c.host_alloc != TKV_HOST_HUGE_ARENA && c.host_alloc != TKV_HOST_PINNED_ALLOC) return TKV_EINVAL;
+    if (c.host_alloc < TKV_HOST_AUTO || c.host_alloc > TKV_HOST_HUGE_ARENA) return TKV_EINVAL;
     const float r[4] = {c.ratio_t0, c.ratio_t1, c.ratio_t2, c.ratio_t3};
     int64_t ppm[4], sum = 0;
     for (int i = 0; i < 4; ++i) {
@@ -1337,6 +1352,8 @@ tkv_status tkv_get_stats(tkv_ctx* ctx, tkv_stats* out) {
     s.attn_splits = ctx->last_splits;
     s.host_huge_bytes = (int64_t)(ctx->hs_h1.huge_bytes + ctx->hs_h2m.huge_bytes + ctx->hs_t2.huge_bytes);
     s.host_numa_node = ctx->host_numa;
+    s.cuda_error = ctx->cuda_error;
+    s.cuda_error_line = ctx->cuda_error_line;
     *out = s;
     return TKV_OK;
 }
