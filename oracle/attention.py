@@ -12,7 +12,7 @@ ARKV summary, "Tri-state cache assignment": quantised tokens are dequantised on
 the fly and concatenated with the others in their original order before
 attention.
 
-Readings (listed in the design doc): softmax scale 1/sqrt(d); evicted tokens are
+Readings where the pages are silent: softmax scale 1/sqrt(d); evicted tokens are
 excluded from both numerator and denominator; under GQA query head h reads KV
 head floor(h / G), G = Hq / Hkv; H in the score equation is the number of query
 heads; the token being decoded is appended before attention and attends to

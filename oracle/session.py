@@ -18,7 +18,7 @@ rather than assume it:
             token promoted out of T2 gets its exact values back
   (T3 tokens are dropped from every container.)
 
-Step semantics (readings listed in the design doc):
+Step semantics (readings where the pages are silent):
   * decode steps are numbered from 1; in step t every sequence appends one new
     position N (into T0: it is inside the recent window) before attention, and
     the new position starts with s = 0;

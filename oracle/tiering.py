@@ -9,7 +9,7 @@ Source: gist.science summary of "Not All Thoughts Need HBM":
   * "System implementation": tiers are re-assigned every Delta = 64 decode
     steps (which amortises the sort).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * the ranking key is (s descending, position ascending): on an exact tie in
     s the lower position ranks higher, so the higher position is evicted
     first;
