@@ -606,6 +606,16 @@ def whole_job_tokens_per_s(batch, steps, world, max_ms):
     return batch * steps * world / (max_ms / 1e3)
 
 
+def hbm_projection(wl, args):
+    """HBM saved by tiering at the end of the run, from the footprint calculator at the
+    workload's shape, batch, token count and tier ratios (steady state)."""
+    from tiered_kv_cache_gqa_gb300 import memory
+    f = memory.projection(wl.num_layers, wl.batch, wl.num_kv_heads, wl.head_dim, wl.max_tokens,
+                          wl.ratios, prompt_len=wl.prompt_len, num_sinks=wl.num_sinks, window=wl.window,
+                          t1_resident=args.t1 == "resident", t2_on_host=args.t2 == "host")
+    return f.saved_bytes
+
+
 def link_fraction(gbs, link):
     """A host-link rate as fractions of the measured link peak and of nominal PCIe Gen5 x16."""
     if gbs is None:
@@ -711,6 +721,7 @@ def main():
             "transfer_overhead_copy_share": link_ms / r["prof_ms"],
             "transfer_overhead_exposed": r["exposed"],
             "hbm_saved_bytes": st["kv_bytes_full_cache"] - st["hbm_bytes_kv_resident"],
+            "hbm_saved_projection_bytes": hbm_projection(wl, args),
             "hbm_kv_resident_bytes": st["hbm_bytes_kv_resident"],
             "kv_full_cache_bytes": st["kv_bytes_full_cache"],
             "tier_count": st["tier_count"],

@@ -36,6 +36,15 @@
  *     TKV_ECAPACITY and every later call except tkv_destroy, tkv_get_stats and
  *     tkv_status_string returns TKV_ESTATE.
  *   - One context is used from one host thread at a time.
+ *   - Fault injection (a test hook for the error paths, host side only): if
+ *     the environment variable TKV_FAULT_INJECT is set when tkv_create runs,
+ *       "hostalloc"  makes that context's pinned host allocations fail
+ *                    (tkv_create returns TKV_ENOMEM and frees what it took);
+ *       "call:N"     makes the N-th checked CUDA call of that context (counted
+ *                    from 1 after creation) report failure after it ran:
+ *                    the call returns TKV_ECUDA, the context is poisoned
+ *                    (tkv_stats.cuda_error = cudaErrorUnknown) and no device
+ *                    work goes wrong.
  *
  * Shapes: L layers, B sequences, Hq query heads, Hkv KV heads, G = Hq / Hkv,
  * d = head_dim (64 or 128).  Query head h reads KV head h / G (GQA).

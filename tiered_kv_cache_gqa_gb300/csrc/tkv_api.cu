@@ -124,6 +124,9 @@ struct tkv_ctx {
     int64_t launches = 0;
     tkv_status status = TKV_OK;
     int cuda_error = 0, cuda_error_line = 0;   // the first failing CUDA call (diagnostics)
+    // host-side fault injection (TKV_FAULT_INJECT, read at creation; a test hook)
+    bool inject_hostalloc = false;
+    int64_t inject_at = 0, inject_count = 0;
     tkv_stats st{};
     size_t hbm_alloc = 0, host_alloc = 0;
 };
@@ -156,13 +159,18 @@ tkv_status fail_cuda(tkv_ctx* c, cudaError_t e, int line) {
     return fail(c, TKV_ECUDA);
 }
 
-#define CK(x)                                                      \
-    do {                                                           \
-        cudaError_t e_ = (x);                                      \
-        if (e_ != cudaSuccess) {                                   \
-            (void)cudaGetLastError();                              \
-            return fail_cuda(ctx, e_, __LINE__);                   \
-        }                                                          \
+// A checked CUDA call made on behalf of a context: the first failure poisons the context.
+// With fault injection on, the inject_at-th checked call is reported as failed
+// (cudaErrorUnknown) after it ran, so no device work goes wrong.
+#define CK(x)                                                                              \
+    do {                                                                                   \
+        cudaError_t e_ = (x);                                                              \
+        if (e_ == cudaSuccess && ctx->inject_at > 0 && ++ctx->inject_count == ctx->inject_at) \
+            e_ = cudaErrorUnknown;                                                         \
+        if (e_ != cudaSuccess) {                                                           \
+            (void)cudaGetLastError();                                                      \
+            return fail_cuda(ctx, e_, __LINE__);                                           \
+        }                                                                                  \
     } while (0)
 
 #define CHECK_CTX()                                        \
@@ -187,9 +195,9 @@ cudaError_t dalloc(tkv_ctx* c, T** p, size_t n) {
 
 template <typename T>
 cudaError_t halloc(tkv_ctx* c, T** p, size_t n) {
-    if (n == 0) {
+    if (n == 0 || c->inject_hostalloc) {
         *p = nullptr;
-        return cudaSuccess;
+        return n == 0 ? cudaSuccess : cudaErrorMemoryAllocation;
     }
     cudaError_t e = cudaHostAlloc((void**)p, n * sizeof(T), cudaHostAllocMapped | cudaHostAllocPortable);
     if (e == cudaSuccess) c->host_alloc += n * sizeof(T);
@@ -295,6 +303,7 @@ char* map_unit(size_t len, size_t align, int numa) {
 cudaError_t harena_alloc(tkv_ctx* c, HostStore& hs, size_t bytes) {
     hs = HostStore();
     if (bytes == 0) return cudaSuccess;
+    if (c->inject_hostalloc) return cudaErrorMemoryAllocation;
     const bool arena = c->cfg.host_alloc == TKV_HOST_HUGE_ARENA ||
                        (c->cfg.host_alloc == TKV_HOST_AUTO && bytes >= ((size_t)1 << 30));
     if (arena) {
@@ -707,6 +716,10 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
     ctx->S2 = c.t2_capacity ? c.t2_capacity : (ppm[2] > 0 ? c.max_tokens : 0);
     for (int i = 0; i < 4; ++i) ctx->ppm[i] = ppm[i];
     ctx->device = c.device;
+    if (const char* fi = std::getenv("TKV_FAULT_INJECT")) {
+        if (std::strcmp(fi, "hostalloc") == 0) ctx->inject_hostalloc = true;
+        else if (std::strncmp(fi, "call:", 5) == 0) ctx->inject_at = std::max(0LL, std::atoll(fi + 5));
+    }
     DeviceGuard guard(c.device);
 
     auto bail = [&](tkv_status s) {
