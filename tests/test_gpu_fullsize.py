@@ -26,11 +26,11 @@ pytestmark = pytest.mark.gpu
 
 CASES = {
     # name: (workload, pre-filled positions (the decoded token adds one), layers, samples,
-    #        fewest CTAs the attention launch must use)
+    #        fewest CTAs the attention launch must use: two per SM for the large ones)
     "7b": ("7b", 2511, None, [(0, 0, 0), (27, 0, 3), (13, 0, 2)], 40),
-    "14b": ("14b", 4095, None, [(0, 0, 0), (47, 7, 7), (23, 3, 5), (11, 5, 2), (36, 1, 4)], 152),
-    "32b": ("32b", 8191, 8, [(0, 0, 0), (7, 3, 7), (4, 2, 5)], 152),
-    "70b": ("70b", 16383, 4, [(0, 0, 0), (3, 7, 7), (2, 4, 3)], 152),
+    "14b": ("14b", 4095, None, [(0, 0, 0), (47, 7, 7), (23, 3, 5), (11, 5, 2), (36, 1, 4)], 304),
+    "32b": ("32b", 8191, 8, [(0, 0, 0), (7, 3, 7), (4, 2, 5)], 304),
+    "70b": ("70b", 16383, 4, [(0, 0, 0), (3, 7, 7), (2, 4, 3)], 304),
 }
 
 

@@ -47,7 +47,8 @@ namespace tkv {
 
 constexpr int kAttnWarps = 4;
 constexpr int kWarpStages = 2;
-constexpr int kMaxWindowRows = 4096;       // retained-list rows a CTA stages in shared memory
+constexpr int kMaxWindowRows = 3584;       // retained-list rows a CTA stages in shared memory
+                                           // (two CTAs of the largest instantiation fit an SM)
 constexpr int kCombineRows = 256;          // alpha rows per combine block (one per thread)
 
 template <int G, int D>
@@ -63,8 +64,11 @@ struct AttnCfg {
     static constexpr int PS = 16 + G * D;            // floats of one (m[8], l[8], O[G][D]) record
     static constexpr size_t off_ring = 0;
     static constexpr size_t off_q = kAttnWarps * sz_warp_ring;
+    // p as (p, p) pairs, one row of PSTR floats per tile row: PSTR * 4 bytes is an odd multiple
+    // of 16, so the lanes that write different rows hit different banks
+    static constexpr int PSTR = 2 * GP + 4;
     static constexpr size_t off_p = off_q + (size_t)G * D * 4;
-    static constexpr size_t off_comb = off_p + (size_t)kAttnWarps * kRows * 2 * GP * 4;   // p as (p, p) pairs
+    static constexpr size_t off_comb = off_p + (size_t)kAttnWarps * kRows * PSTR * 4;
     static constexpr size_t off_n = off_comb + (size_t)kAttnWarps * PS * 4;   // rows of each item
     // per item: rows, decode-token flag, (sequence << 16 | KV head)
     static constexpr size_t off_rl = off_n + (size_t)(kMaxWindowRows / 128) * 3 * 4;
@@ -86,7 +90,11 @@ __device__ __forceinline__ void cp_async_wait_prev() {
 template <int G, int D, bool COMPACT>
 __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
-    constexpr int GP = C::GP, ROWB = C::ROWB, CPL = C::CPL, PS = C::PS;
+    constexpr int GP = C::GP, ROWB = C::ROWB, CPL = C::CPL, PS = C::PS, PSTR = C::PSTR;
+    // QK lane map: a lane takes rows (lane & 15) and (lane & 15) + 16 of a tile and the query
+    // heads of its half-warp: heads [0, GH) for lanes 0-15, [GH, G) for lanes 16-31.  Each q
+    // element read from shared memory then feeds two rows.
+    constexpr int GH = (G + 1) / 2;
     constexpr int kQKUnroll = COMPACT ? 4 : D / 8;      // chunks of 8 elements of a K row
     constexpr int kPVUnroll = COMPACT ? 4 : kRows;      // rows of a V tile
     constexpr int kIssueUnroll = COMPACT ? 4 : 8;
@@ -108,7 +116,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     const int it1 = min(total_items, it0 + a.items_per_cta);
     if (it0 >= it1) return;
     uint8_t* ring = smem + C::off_ring + (size_t)warp * C::sz_warp_ring;
-    float* p_s = reinterpret_cast<float*>(smem + C::off_p) + (size_t)warp * kRows * 2 * GP;
+    float* p_s = reinterpret_cast<float*>(smem + C::off_p) + (size_t)warp * kRows * C::PSTR;
 
     // Prologue in one round trip: the rows of every item, the retained-list slices
     // (read up to the item size, clamped to the capacity; entries past the count
@@ -256,29 +264,37 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     int consumed = 0;
 
     // ---------------------------------------------------- per-warp segment state
-    float m_w[G], l_l[G];
+    const int rp = lane & 15, hg = lane >> 4;
+    const int hbase = hg * GH;                       // first head of this lane's half-warp
+    const int nh = hg ? G - GH : GH;                 // heads of this lane's half-warp
+    float m_w[G], l_g[GH];                           // running max (all heads); sum of p (own heads)
     float2 o[G][CPL / 2];
     auto reset_segment = [&]() {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             m_w[h] = -INFINITY;
-            l_l[h] = 0.f;
 #pragma unroll
             for (int c = 0; c < CPL / 2; ++c) o[h][c] = make_float2(0.f, 0.f);
         }
+#pragma unroll
+        for (int h = 0; h < GH; ++h) l_g[h] = 0.f;
     };
     // merges the four warps' (m, l, O) of group g into this CTA's partial record for g
     auto flush_segment = [&](int g) {
         float* cw = comb + (size_t)warp * PS;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float l = l_l[h];
+        for (int h = 0; h < GH; ++h) {
+            // sum over the half-warp that owns head hbase + h
+            float l = l_g[h];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            if (lane == h) {
-                cw[h] = m_w[h];
-                cw[8 + h] = l;
-            }
+            for (int off = 8; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (rp == 0 && h < nh) cw[8 + hbase + h] = l;
+        }
+        if (lane < G) {
+            float m = m_w[0];
+#pragma unroll
+            for (int h = 1; h < G; ++h) m = lane == h ? m_w[h] : m;
+            cw[lane] = m;
         }
 #pragma unroll
         for (int h = 0; h < G; ++h)
@@ -329,8 +345,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         float* zg = a.zs + (((size_t)b * a.Hkv + kvh) * a.Nmax + j0) * GP;
         for (int k = 0; k < nt; ++k) {
             const int tile = warp + kAttnWarps * k;
-            const int jl = tile * kRows + lane;
-            const bool valid = jl < n;
+            const int ra = rp, rb = rp + 16;           // this lane's rows in the tile
+            const int ja = tile * kRows + ra, jb = tile * kRows + rb;
+            const bool valid_a = ja < n, valid_b = jb < n;
 
             // ---------------------------------------------------------- K tile
             issue_next();                       // the V tile of this tile
@@ -350,101 +367,153 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                 }
             };
             if (newr >= 0) store_new_row(0);
-            float z[G];
+            float za[GH], zb[GH];
+            {
+                const uint8_t* stage_k = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
+                const uint8_t* row_a = stage_k + (size_t)ra * ROWB;
+                const uint8_t* row_b = stage_k + (size_t)rb * ROWB;
+                // two independent accumulator pairs per (row, head): (k0, k2) and (k1, k3) of each chunk
+                float2 acca[GH], acca2[GH], accb[GH], accb2[GH];
 #pragma unroll
-            for (int h = 0; h < G; ++h) z[h] = -INFINITY;
-            if (valid) {
-                const uint8_t* row = ring + (size_t)(consumed % kWarpStages) * C::sz_stage + (size_t)lane * ROWB;
-                // two independent accumulator pairs per head: (k0, k2) and (k1, k3) of each chunk
-                float2 acc[G], acc2[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) acc[h] = acc2[h] = make_float2(0.f, 0.f);
-                float zscale = 1.0f;
-                if (tmask != 0u) {
-                    // a tile with T2 rows: lanes load and convert their own kind of row, the
-                    // FMAs are shared (no serialised second pass over the chunk loop)
-                    const bool f8 = (tmask >> lane) & 1u;
-                    if (f8) zscale = *reinterpret_cast<const float*>(row + D);
-#pragma unroll 4
-                    for (int c = 0; c < D / 8; ++c) {
-                        float2 k0, k1, k2, k3;
-                        if (!f8) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
-                            k0 = bf16x2_to_float2(w.x);
-                            k1 = bf16x2_to_float2(w.y);
-                            k2 = bf16x2_to_float2(w.z);
-                            k3 = bf16x2_to_float2(w.w);
-                        } else {
-                            const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
-                            k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
-                            k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
-                            k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
-                            k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
-                        }
-#pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
-                            const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
-                            acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
-                            acc2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[h]);
-                            acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
-                            acc2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[h]);
-                        }
-                    }
-                } else {
-#pragma unroll kQKUnroll
-                    for (int c = 0; c < D / 8; ++c) {
+                for (int h = 0; h < GH; ++h) acca[h] = acca2[h] = accb[h] = accb2[h] = make_float2(0.f, 0.f);
+                // eight elements of a row from its chunk c: bf16, or E4M3 codes of a T2 record
+                auto load8 = [&](const uint8_t* row, bool f8, int c, float2& k0, float2& k1, float2& k2, float2& k3) {
+                    if (!f8) {
                         const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
-                        const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
-                        const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+                        k0 = bf16x2_to_float2(w.x);
+                        k1 = bf16x2_to_float2(w.y);
+                        k2 = bf16x2_to_float2(w.z);
+                        k3 = bf16x2_to_float2(w.w);
+                    } else {
+                        const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
+                        k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
+                        k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
+                        k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
+                        k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
+                    }
+                };
+                auto qk_chunk = [&](int c, bool fa, bool fb) {
+                    float2 a0, a1, a2, a3, b0, b1, b2, b3;
+                    load8(row_a, fa, c, a0, a1, a2, a3);
+                    load8(row_b, fb, c, b0, b1, b2, b3);
 #pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
-                            const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
-                            acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[h]);
-                            acc2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc2[h]);
-                            acc[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[h]);
-                            acc2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc2[h]);
+                    for (int h = 0; h < GH; ++h) {
+                        // heads past G (the short half-warp of an odd G) read head G - 1; discarded
+                        const float* qh = q_s + (size_t)min(hbase + h, G - 1) * D + c * 8;
+                        const float4 qa = *reinterpret_cast<const float4*>(qh);
+                        const float4 qb = *reinterpret_cast<const float4*>(qh + 4);
+                        acca[h] = __ffma2_rn(make_float2(qa.x, qa.y), a0, acca[h]);
+                        accb[h] = __ffma2_rn(make_float2(qa.x, qa.y), b0, accb[h]);
+                        acca2[h] = __ffma2_rn(make_float2(qa.z, qa.w), a1, acca2[h]);
+                        accb2[h] = __ffma2_rn(make_float2(qa.z, qa.w), b1, accb2[h]);
+                        acca[h] = __ffma2_rn(make_float2(qb.x, qb.y), a2, acca[h]);
+                        accb[h] = __ffma2_rn(make_float2(qb.x, qb.y), b2, accb[h]);
+                        acca2[h] = __ffma2_rn(make_float2(qb.z, qb.w), a3, acca2[h]);
+                        accb2[h] = __ffma2_rn(make_float2(qb.z, qb.w), b3, accb2[h]);
+                    }
+                };
+                float sca = 1.0f, scb = 1.0f;
+                if (tmask != 0u) {
+                    // A tile with T2 rows: every T2 record of the stage is widened in place to a
+                    // bf16 row (E4M3 values are exact in bf16), one row per lane -- row ra by
+                    // the lanes 0-15, row rb by the lanes 16-31 -- and its scale kept aside; the
+                    // dot products then run the bf16 loop and are scaled after it.
+                    uint8_t* mine = const_cast<uint8_t*>(hg ? row_b : row_a);
+                    float my_sc = 1.0f;
+                    if ((tmask >> (hg ? rb : ra)) & 1u) {
+                        my_sc = *reinterpret_cast<const float*>(mine + D);
+                        uint4 codes[D / 16];
+#pragma unroll
+                        for (int c = 0; c < D / 16; ++c) codes[c] = reinterpret_cast<const uint4*>(mine)[c];
+#pragma unroll
+                        for (int c = 0; c < D / 16; ++c) {
+                            const uint32_t w[4] = {codes[c].x, codes[c].y, codes[c].z, codes[c].w};
+                            uint32_t outw[8];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 lo = e4m3x2_to_float2((uint16_t)(w[i] & 0xFFFF));
+                                const float2 hi = e4m3x2_to_float2((uint16_t)(w[i] >> 16));
+                                const __nv_bfloat162 blo = __floats2bfloat162_rn(lo.x, lo.y);
+                                const __nv_bfloat162 bhi = __floats2bfloat162_rn(hi.x, hi.y);
+                                outw[2 * i] = *reinterpret_cast<const uint32_t*>(&blo);
+                                outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bhi);
+                            }
+                            reinterpret_cast<uint4*>(mine)[2 * c] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+                            reinterpret_cast<uint4*>(mine)[2 * c + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
                         }
                     }
+                    __syncwarp();
+                    // the scale of row ra sits with lane ra, that of row rb with lane 16 + rb - 16
+                    sca = __shfl_sync(0xffffffffu, my_sc, rp);
+                    scb = __shfl_sync(0xffffffffu, my_sc, 16 + rp);
                 }
+#pragma unroll kQKUnroll
+                for (int c = 0; c < D / 8; ++c) qk_chunk(c, false, false);
 #pragma unroll
-                for (int h = 0; h < G; ++h) z[h] = ((acc[h].x + acc[h].y) + (acc2[h].x + acc2[h].y)) * zscale;
+                for (int h = 0; h < GH; ++h) {
+                    const bool live = h < nh;
+                    za[h] = (valid_a && live) ? ((acca[h].x + acca[h].y) + (acca2[h].x + acca2[h].y)) * sca : -INFINITY;
+                    zb[h] = (valid_b && live) ? ((accb[h].x + accb[h].y) + (accb2[h].x + accb2[h].y)) * scb : -INFINITY;
+                }
             }
             __syncwarp();
             ++consumed;
 
             // ------------------------------ online softmax update (warp-uniform max)
-            float p[GP];
+            // tile maxima of this half-warp's heads, then the other half-warp's by one exchange
+            float tmax[G];
 #pragma unroll
-            for (int h = 0; h < GP; ++h) p[h] = 0.f;
+            for (int h = 0; h < GH; ++h) {
+                float tm = fmaxf(za[h], zb[h]);
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
+                const float other = __shfl_xor_sync(0xffffffffu, tm, 16);
+                tmax[h] = hg ? other : tm;
+                if (GH + h < G) tmax[GH + h] = hg ? tm : other;
+            }
+            float sc_all[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float tm = z[h];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
-                const float m_new = fmaxf(m_w[h], tm);
-                const float sc = (m_w[h] == -INFINITY) ? 0.f : exp2f(m_w[h] - m_new);
+                const float m_new = fmaxf(m_w[h], tmax[h]);
+                sc_all[h] = (m_w[h] == -INFINITY) ? 0.f : exp2f(m_w[h] - m_new);
                 m_w[h] = m_new;
-                l_l[h] *= sc;
 #pragma unroll
-                for (int c = 0; c < CPL / 2; ++c) o[h][c] = __fmul2_rn(o[h][c], make_float2(sc, sc));
-                if (valid) {
-                    p[h] = exp2f(z[h] - m_new);
-                    l_l[h] += p[h];
+                for (int c = 0; c < CPL / 2; ++c) o[h][c] = __fmul2_rn(o[h][c], make_float2(sc_all[h], sc_all[h]));
+            }
+            float pa[GH], pb[GH];
+#pragma unroll
+            for (int h = 0; h < GH; ++h) {
+                // this lane's head hbase + h: its scale and new max, selected without indexing
+                const float sc = (hg && GH + h < G) ? sc_all[GH + h < G ? GH + h : 0] : sc_all[h];
+                const float mh = (hg && GH + h < G) ? m_w[GH + h < G ? GH + h : 0] : m_w[h];
+                l_g[h] *= sc;
+                pa[h] = za[h] == -INFINITY ? 0.f : exp2f(za[h] - mh);
+                pb[h] = zb[h] == -INFINITY ? 0.f : exp2f(zb[h] - mh);
+                l_g[h] += pa[h];
+                l_g[h] += pb[h];
+            }
+            // p as (p, p) pairs of this lane's heads, rows ra and rb
+#pragma unroll
+            for (int h = 0; h < GH; ++h) {
+                if (h < nh) {
+                    *reinterpret_cast<float2*>(p_s + (size_t)ra * PSTR + 2 * (hbase + h)) = make_float2(pa[h], pa[h]);
+                    *reinterpret_cast<float2*>(p_s + (size_t)rb * PSTR + 2 * (hbase + h)) = make_float2(pb[h], pb[h]);
                 }
             }
+            // logits of this lane's heads for the alpha sums (slots of heads past G are never read)
+            auto store_z = [&](float* dst, const float* z) {
+                if constexpr (GH == 4) {
+                    *reinterpret_cast<float4*>(dst) = make_float4(z[0], z[1], z[2], z[3]);
+                } else if constexpr (GH == 2) {
+                    *reinterpret_cast<float2*>(dst) = make_float2(z[0], z[1]);
+                } else {
 #pragma unroll
-            for (int h = 0; h < GP; h += 2)
-                *reinterpret_cast<float4*>(p_s + (size_t)lane * 2 * GP + 2 * h) = make_float4(p[h], p[h], p[h + 1], p[h + 1]);
-            if (valid) {
-                float zz[GP];
-#pragma unroll
-                for (int h = 0; h < GP; ++h) zz[h] = h < G ? z[h] : 0.f;
-#pragma unroll
-                for (int h = 0; h < GP; h += 4)
-                    *reinterpret_cast<float4*>(zg + (size_t)jl * GP + h) = make_float4(zz[h], zz[h + 1], zz[h + 2], zz[h + 3]);
-            }
+                    for (int h = 0; h < GH; ++h)
+                        if (h < nh) dst[h] = z[h];
+                }
+            };
+            if (valid_a) store_z(zg + (size_t)ja * GP + hbase, za);
+            if (valid_b) store_z(zg + (size_t)jb * GP + hbase, zb);
             __syncwarp();
 
             // ---------------------------------------------------------- V tile
@@ -462,7 +531,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                     float2 pp[G];
 #pragma unroll
                     for (int h = 0; h < G; h += 2) {
-                        const float4 t = *reinterpret_cast<const float4*>(p_s + (size_t)r * 2 * GP + 2 * h);
+                        const float4 t = *reinterpret_cast<const float4*>(p_s + (size_t)r * PSTR + 2 * h);
                         pp[h] = make_float2(t.x, t.y);
                         if (h + 1 < G) pp[h + 1] = make_float2(t.z, t.w);
                     }
@@ -708,6 +777,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st) {
     if (a.d == 64) { TKV_DISPATCH_G(64, launch_gd, a, st) }
     return cudaErrorInvalidValue;
 }
+
+int attention_max_window_rows() { return kMaxWindowRows; }
 
 size_t attention_smem_bytes(int G, int d, int rl_rows) {
     if (d == 128) { TKV_DISPATCH_G(128, smem_gd, rl_rows) }

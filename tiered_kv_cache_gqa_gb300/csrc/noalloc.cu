@@ -112,7 +112,7 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
     const int G = Hq / Hkv;
 
     // same launch plan as the context path
-    const size_t smem_max = attention_smem_bytes(G, d, 4096);
+    const size_t smem_max = attention_smem_bytes(G, d, attention_max_window_rows());
     if (attention_ensure_smem(G, d, smem_max) != cudaSuccess) {
         (void)cudaGetLastError();
         return TKV_ECUDA;

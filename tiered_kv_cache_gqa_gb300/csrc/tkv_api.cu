@@ -840,9 +840,9 @@ tkv_status tkv_create(const tkv_config* cfg, tkv_ctx** out) {
         return bail(TKV_ECUDA);
     }
 
-    // kernel set-up: the largest attention launch stages 4096 retained rows per CTA
+    // kernel set-up: the largest attention launch stages a full retained-list window per CTA
     {
-        const size_t smem = attention_smem_bytes(G, ctx->d, 4096);
+        const size_t smem = attention_smem_bytes(G, ctx->d, attention_max_window_rows());
         if (attention_prepare(G, ctx->d, smem) != cudaSuccess) return bail(TKV_ECUDA);
         ctx->resident = attention_resident_ctas(G, ctx->d, smem);
         if (ctx->resident < 1) return bail(TKV_ECUDA);

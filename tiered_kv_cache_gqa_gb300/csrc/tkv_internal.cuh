@@ -123,6 +123,7 @@ size_t attention_zs_floats(int G, int B, int Hkv, int Nmax);
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
 size_t attention_smem_bytes(int G, int d, int rl_rows);
+int attention_max_window_rows();                                // retained rows a CTA can stage
 cudaError_t attention_prepare(int G, int d, size_t smem);
 int attention_resident_ctas(int G, int d, size_t smem);                  // CTAs per device
 cudaError_t attention_ensure_smem(int G, int d, size_t smem);   // raises the cap, never lowers it
