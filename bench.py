@@ -673,7 +673,7 @@ def main():
         hbm_peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     except Exception:
         hbm_peak, peak_src = 6800.0, "fallback"
-    pa, p1, pd = r["prof"]["attn"], r["prof"]["t1"], r["prof"]["delta"]
+    pa, pc, p1, pd = r["prof"]["attn"], r["prof"]["combine"], r["prof"]["t1"], r["prof"]["delta"]
     KP_ = r["prof_steps"]
     # DRAM bytes per launch: the ncu-measured ratio to the algorithmic bytes, scaled to this
     # run's launches (traffic grows with the retained rows a launch reads)
@@ -695,7 +695,9 @@ def main():
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "kernel": "tkv::attn_kernel", "peak_source": peak_src,
                      "launches": pa["count"], "avg_launch_us": 1e3 * pa["ms"] / max(1, pa["count"]),
-                     "bytes_per_launch": pa["bytes"] / max(1, pa["count"])},
+                     "bytes_per_launch": pa["bytes"] / max(1, pa["count"]),
+                     "note": "main attention kernel alone (CUDA events on the compute stream, eager "
+                             "profiled steps); the combine kernel that follows it is in detail.attention_combine"},
         "cpu_baseline": cpu,
         "e2e": ({"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                  "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"]}
@@ -709,7 +711,11 @@ def main():
             "profiled_pass": {"steps": KP_, "first_step": tl["prof0"], "mode": "eager",
                               "ms_per_step": r["prof_ms"] / KP_,
                               "note": "per-kernel events; roofline and transfer figures come from this pass"},
-            "attention_step_ms": pa["ms"] / KP_,
+            "attention_step_ms": (pa["ms"] + pc["ms"]) / KP_,
+            "attention_combine": {"avg_launch_us": 1e3 * pc["ms"] / max(1, pc["count"]),
+                                  "launches": pc["count"], "bytes_per_launch": pc["bytes"] / max(1, pc["count"]),
+                                  "pair_frac_of_hbm_peak": ((pa["bytes"] + pc["bytes"]) / ((pa["ms"] + pc["ms"]) / 1e3)
+                                                            / 1e9 / hbm_peak) if pa["ms"] + pc["ms"] > 0 else None},
             "host_link_measured": r["link"],
             "host_stores": {"bytes": st["host_bytes_allocated"], "huge_page_bytes": st["host_huge_bytes"],
                             "numa_node": st["host_numa_node"]},

@@ -286,10 +286,15 @@ typedef struct {
 
 /* Kernel and copy timing.  tkv_profile_begin clears the counters and, until
  * tkv_profile_end, brackets with CUDA events (at most 16384 of each kind):
- *   attn   -- every attention launch, on the compute stream, right around the
- *             kernel (after its wait for the T1 fetch).  Bytes per launch and
- *             sequence: 4*Hkv*d per T0/T1 row, 2*Hkv*d + 8*Hkv per T2 row
- *             (codes + two fp32 scales), plus q (bf16) and out (fp32);
+ *   attn   -- every launch of the attention main kernel, on the compute
+ *             stream, right around the kernel (after its wait for the T1
+ *             fetch).  Bytes per launch and sequence: 4*Hkv*d per T0/T1 row,
+ *             2*Hkv*d + 8*Hkv per T2 row (codes + two fp32 scales), plus q
+ *             (bf16);
+ *   combine -- every launch of the attention combine kernel that follows it
+ *             (the bracket between the two kernels keeps them from
+ *             overlapping while timed); bytes: out (fp32) plus, per retained
+ *             row and KV head, its logits and its alpha running sum;
  *   t1     -- every per-layer T1 copy (pinned host -> HBM staging) on the
  *             copy stream; bytes = rows copied * 4*Hkv*d;
  *   delta  -- every delta-prefetch gather of promoted rows on the copy stream;
@@ -297,8 +302,8 @@ typedef struct {
  * tkv_profile_end synchronises, stops recording and fills the entries (any
  * pointer may be NULL). */
 tkv_status tkv_profile_begin(tkv_ctx* ctx);
-tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t1,
-                           tkv_prof_entry* delta);
+tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* combine,
+                           tkv_prof_entry* t1, tkv_prof_entry* delta);
 
 /* Allocation-free decode step for callers that cannot let a library allocate
  * device memory: runtimes whose caching allocator owns the whole memory

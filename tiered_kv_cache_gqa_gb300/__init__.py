@@ -116,7 +116,7 @@ def load():
     lib.tkv_get_row.argtypes = [vp, i32, i32, i32, vp, vp, ctypes.POINTER(i32)]
     lib.tkv_profile_begin.argtypes = [vp]
     lib.tkv_profile_end.argtypes = [vp, ctypes.POINTER(ProfEntry), ctypes.POINTER(ProfEntry),
-                                    ctypes.POINTER(ProfEntry)]
+                                    ctypes.POINTER(ProfEntry), ctypes.POINTER(ProfEntry)]
     lib.tkv_decode_dense_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.tkv_capture_begin.argtypes = [vp]
     lib.tkv_capture_end.argtypes = [vp, ctypes.POINTER(i32)]
@@ -226,10 +226,11 @@ def tkv_profile_begin(ctx):
 
 
 def tkv_profile_end(ctx):
-    """Returns (status, {"attn": ..., "t1": ..., "delta": ...}) of ProfEntry dicts."""
-    e = [ProfEntry(), ProfEntry(), ProfEntry()]
-    rc = load().tkv_profile_end(ctx, ctypes.byref(e[0]), ctypes.byref(e[1]), ctypes.byref(e[2]))
-    return rc, {"attn": e[0].as_dict(), "t1": e[1].as_dict(), "delta": e[2].as_dict()}
+    """Returns (status, {"attn": ..., "combine": ..., "t1": ..., "delta": ...}) of ProfEntry dicts."""
+    e = [ProfEntry(), ProfEntry(), ProfEntry(), ProfEntry()]
+    rc = load().tkv_profile_end(ctx, *(ctypes.byref(x) for x in e))
+    return rc, {"attn": e[0].as_dict(), "combine": e[1].as_dict(), "t1": e[2].as_dict(),
+                "delta": e[3].as_dict()}
 
 
 def tkv_decode_dense_noalloc(q, kv, out, s, num_layers, batch, num_q_heads, num_kv_heads,

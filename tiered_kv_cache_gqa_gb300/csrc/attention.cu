@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) 
 
 // ------------------------------------------------------------------ dispatch
 template <int G, int D>
-static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
+static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st, cudaEvent_t after_main, cudaEvent_t before_combine) {
     using C = AttnCfg<G, D>;
     const size_t smem = C::smem(a.items_per_cta * a.item_rows);
     // at most two tiles per warp: the compact instantiation
@@ -696,6 +696,8 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st) {
         attn_kernel<G, D, false><<<a.grid, kAttnWarps * 32, smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (after_main && (e = cudaEventRecord(after_main, st)) != cudaSuccess) return e;
+    if (before_combine && (e = cudaEventRecord(before_combine, st)) != cudaSuccess) return e;
     // one alpha row per thread; enough blocks that every block holds at most 256 out elements
     const int rows = a.items_per_group * a.item_rows;
     const int blocks = std::max((rows + kCombineRows - 1) / kCombineRows, (G * D + kCombineRows - 1) / kCombineRows);
@@ -771,10 +773,10 @@ static cudaError_t ensure_smem_gd(size_t smem) {
         default: break;                                 \
     }
 
-cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, cudaEvent_t after_main, cudaEvent_t before_combine) {
     const int G = a.Hq / a.Hkv;
-    if (a.d == 128) { TKV_DISPATCH_G(128, launch_gd, a, st) }
-    if (a.d == 64) { TKV_DISPATCH_G(64, launch_gd, a, st) }
+    if (a.d == 128) { TKV_DISPATCH_G(128, launch_gd, a, st, after_main, before_combine) }
+    if (a.d == 64) { TKV_DISPATCH_G(64, launch_gd, a, st, after_main, before_combine) }
     return cudaErrorInvalidValue;
 }
 

@@ -115,11 +115,13 @@ struct tkv_ctx {
     int resident = 1;                  // attention CTAs resident on the device at once
     int last_splits = 0;
 
-    // timing (tkv_profile_begin / tkv_profile_end): kinds 0 attention, 1 T1 copy, 2 delta
+    // timing (tkv_profile_begin / tkv_profile_end): kinds 0 attention main kernel, 1 T1 copy,
+    // 2 delta, 3 attention combine kernel
+    static constexpr int kProfKinds = 4;
     static constexpr int kProfPairs = 16384;
-    std::vector<cudaEvent_t> prof_ev[3];   // 2 per pair, created on first use
-    int prof_used[3] = {0, 0, 0};
-    double prof_bytes[3] = {0, 0, 0};
+    std::vector<cudaEvent_t> prof_ev[kProfKinds];   // 2 per pair, created on first use
+    int prof_used[kProfKinds] = {0, 0, 0, 0};
+    double prof_bytes[kProfKinds] = {0, 0, 0, 0};
     bool profiling = false;
     int64_t launches = 0;
     tkv_status status = TKV_OK;
@@ -981,14 +983,29 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
     a.part_per_group = plan.part_per_group;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)ctx->d));
     const bool timed = prof_open(ctx, 0, ctx->compute);
-    CK(launch_attention(a, ctx->compute));
+    // when timed, the main kernel and the combine kernel are bracketed separately
+    cudaEvent_t mid0 = nullptr, mid1 = nullptr;
+    if (timed) {
+        mid0 = ctx->prof_ev[0][2 * ctx->prof_used[0] + 1];
+        mid1 = ctx->prof_used[3] < tkv_ctx::kProfPairs ? ctx->prof_ev[3][2 * ctx->prof_used[3]] : nullptr;
+    }
+    CK(launch_attention(a, ctx->compute, mid0, mid1));
     ctx->launches += 2;
     if (timed) {
-        double bytes = (double)ctx->B * ctx->Hq * ctx->d * (2 + 4);
+        // main kernel: the K/V rows it reads (bf16 rows of T0 / T1, T2 codes + scales) and q
+        double bytes = (double)ctx->B * ctx->Hq * ctx->d * 2;
         for (int b = 0; b < ctx->B; ++b)
             bytes += (double)(ctx->count[0][b] + ctx->count[1][b]) * 4.0 * ctx->Hkv * ctx->d +
                      (double)ctx->count[2][b] * (2.0 * ctx->Hkv * ctx->d + 8.0 * ctx->Hkv);
-        prof_close(ctx, 0, ctx->compute, bytes);
+        ctx->prof_used[0]++;
+        ctx->prof_bytes[0] += bytes;
+        if (mid1) {
+            // combine: out (fp32) written, the logits and alpha sums of the retained rows
+            double cb = (double)ctx->B * ctx->Hq * ctx->d * 4;
+            const int GP = ctx->G <= 4 ? 4 : 8;
+            for (int b = 0; b < ctx->B; ++b) cb += (double)ctx->R[b] * ctx->Hkv * (GP * 4.0 + 8.0);
+            prof_close(ctx, 3, ctx->compute, cb);
+        }
     }
     CK(cudaEventRecord(ctx->ev_attn[slotr], ctx->compute));
     if (ctx->capturing) {
@@ -1126,7 +1143,7 @@ tkv_status tkv_profile_begin(tkv_ctx* ctx) {
     CHECK_CTX();
     if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     DeviceGuard guard(ctx->device);
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < tkv_ctx::kProfKinds; ++k) {
         if (ctx->prof_ev[k].empty()) {
             ctx->prof_ev[k].resize(2 * tkv_ctx::kProfPairs, nullptr);
             for (auto& e : ctx->prof_ev[k]) CK(cudaEventCreate(&e));
@@ -1138,15 +1155,16 @@ tkv_status tkv_profile_begin(tkv_ctx* ctx) {
     return TKV_OK;
 }
 
-tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* t1, tkv_prof_entry* delta) {
+tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* combine, tkv_prof_entry* t1,
+                           tkv_prof_entry* delta) {
     CHECK_CTX();
     if (ctx->capturing) return TKV_EINVAL;   // synchronous: not inside a capture
     DeviceGuard guard(ctx->device);
     ctx->profiling = false;
     CK(cudaStreamSynchronize(ctx->copy));
     CK(cudaStreamSynchronize(ctx->compute));
-    tkv_prof_entry* outs[3] = {attn, t1, delta};
-    for (int k = 0; k < 3; ++k) {
+    tkv_prof_entry* outs[tkv_ctx::kProfKinds] = {attn, t1, delta, combine};
+    for (int k = 0; k < tkv_ctx::kProfKinds; ++k) {
         double ms = 0.0;
         for (int i = 0; i < ctx->prof_used[k]; ++i) {
             float t = 0.f;

@@ -121,7 +121,10 @@ AttnPlan attention_plan(int G, int d, int B, int Hkv, int rmax, int resident);
 size_t attention_part_floats(int G, int d, int B, int Hkv, int Nmax, int resident);   // scratch sizes
 size_t attention_zs_floats(int G, int B, int Hkv, int Nmax);
 
-cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st);
+// Launches the main kernel and the combine kernel.  If given, `after_main` is recorded between
+// the two launches and `before_combine` right after it (event timing of each kernel).
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t st, cudaEvent_t after_main = nullptr,
+                             cudaEvent_t before_combine = nullptr);
 size_t attention_smem_bytes(int G, int d, int rl_rows);
 int attention_max_window_rows();                                // retained rows a CTA can stage
 cudaError_t attention_prepare(int G, int d, size_t smem);
