@@ -612,9 +612,13 @@ __global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) 
     const int i0 = blockIdx.x * per, i1 = min(G * D, i0 + per);
     const int idx = i0 + threadIdx.x;                // blockDim.x >= per: one element per thread
     const bool has_out = idx < i1;
+    // only the warps that hold out elements load partial outputs (a warp-uniform branch); the
+    // values are used in step (3) by the same threads only
     float v[kSegBatch];
+    if (i0 + (int)(threadIdx.x & ~31u) < i1) {
 #pragma unroll
-    for (int k = 0; k < kSegBatch; ++k) v[k] = (has_out && k < ns) ? rec(k)[16 + idx] : 0.f;
+        for (int k = 0; k < kSegBatch; ++k) v[k] = (has_out && k < ns) ? rec(k)[16 + idx] : 0.f;
+    }
     const int j = blockIdx.x * kCombineRows + threadIdx.x;
     const bool has_row = j < a.Nmax;
     float zz[GP];
