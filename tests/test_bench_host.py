@@ -70,3 +70,28 @@ def test_reference_arm_runs_on_cpu_and_prints_its_line():
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["higher_is_better"] is True
+
+
+def test_timed_window_holds_a_retier_and_the_delta_step():
+    """The timed steps contain a re-tier step (t % 64 == 0) and the delta-prefetch step after it,
+    the profiled pass starts right after the second re-tier, and the last timed step ends the
+    configuration's sequence."""
+    for steps, warmup in ((20, 5), (2, 1), (64, 3), (512, 3)):
+        tl = bench.timeline(steps, warmup)
+        timed = range(tl["timed0"], tl["last"] + 1)
+        assert len(timed) == steps and tl["timed0"] - tl["warm0"] == warmup
+        assert tl["prof0"] == bench.PRE_STEPS + 1 and tl["fill0"] == tl["prof0"] + tl["kp"]
+        assert tl["warm0"] >= tl["fill0"]
+        r = [t for t in timed if t % 64 == 0]
+        assert r and r[0] + 1 in timed and tl["retiers_timed"] == r
+    for name in ("7b", "14b", "32b", "70b"):
+        wl = bench.bench_workload(name, 5, 20)
+        assert wl.prefill_len + wl.decode_steps == bench.TARGET_N[name]
+
+
+def test_both_arms_describe_the_same_config():
+    args = bench.parse(["--workload", "70b", "--steps", "20", "--warmup", "5"])
+    wl = bench.bench_workload(args.workload, args.warmup, args.steps)
+    ref = bench.parse(["--impl", "reference", "--workload", "70b", "--steps", "20", "--warmup", "5"])
+    assert bench.run_config(args, wl) == bench.run_config(ref, bench.bench_workload("70b", 5, 20))
+    assert bench.run_config(args, wl)["retier_steps_timed"] == [192]
