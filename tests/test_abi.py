@@ -78,3 +78,10 @@ def header_struct_fields(name):
 def test_binding_structs_match_the_header(cname, pyname):
     import tiered_kv_cache_gqa_gb300 as tkv
     assert [f[0] for f in getattr(tkv, pyname)._fields_] == header_struct_fields(cname)
+
+
+def test_host_link_probe_rejects_bad_sizes_without_a_gpu(lib_path):
+    import tiered_kv_cache_gqa_gb300 as tkv
+    assert tkv.tkv_measure_host_link(0, 1000)[0] == tkv.TKV_EINVAL          # below 1 MiB
+    assert tkv.tkv_measure_host_link(0, (1 << 20) + 8)[0] == tkv.TKV_EINVAL  # not a multiple of 16
+    assert tkv.tkv_measure_host_link(-1, 1 << 20)[0] == tkv.TKV_EINVAL

@@ -39,3 +39,10 @@ def test_calculator_matches_the_library_accounting(t1, t2):
     assert st["hbm_bytes_kv_resident"] == f.resident_bytes
     # the re-tier hands out dense T1 slots: one staged layer holds exactly the T1 rows
     assert st["t1_rows_streamed"] == max(c[1] for c in counts)
+
+
+def test_host_link_probe_reports_the_three_paths():
+    rc, link = tkv.tkv_measure_host_link(0, 64 << 20)
+    assert rc == tkv.TKV_OK
+    for k in ("h2d_ce_gbs", "h2d_sm_gbs", "d2h_ce_gbs"):
+        assert 1.0 < link[k] < 2000.0, (k, link[k])

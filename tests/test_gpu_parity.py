@@ -36,6 +36,10 @@ SHAPES = {
     "g7_d128": (2, 28, 4, 128, 1, 1100, 66, (0.30, 0.67, 0.0, 0.03), 0.0),
     "g8_d128_long": (1, 64, 8, 128, 1, 2100, 65, (0.30, 0.60, 0.05, 0.05), 0.001),
     "g1_d64": (1, 3, 3, 64, 3, 300, 66, (0.5, 0.3, 0.1, 0.1), 0.0),
+    # odd and even half-warp head splits: G = 3 (2 + 1 heads), G = 6 (3 + 3), G = 8 at d 64
+    "g3_d64_b2": (2, 6, 2, 64, 2, 500, 66, (0.4, 0.4, 0.1, 0.1), 0.005),
+    "g6_d128": (1, 24, 4, 128, 1, 800, 66, (0.3, 0.6, 0.05, 0.05), 0.0),
+    "g8_d64_b2": (1, 16, 2, 64, 2, 700, 66, (0.3, 0.5, 0.15, 0.05), 0.01),
 }
 
 
