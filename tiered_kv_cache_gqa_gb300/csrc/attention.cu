@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     // heads of its half-warp: heads [0, GH) for lanes 0-15, [GH, G) for lanes 16-31.  Each q
     // element read from shared memory then feeds two rows.
     constexpr int GH = (G + 1) / 2;
-    constexpr int kQKUnroll = COMPACT ? 4 : D / 8;      // chunks of 8 elements of a K row
+    constexpr int kQKUnroll = COMPACT ? 4 : 8;          // chunks of 8 elements of a K row (half a row:
+                                                        // a smaller loop body, fewer instruction-cache misses)
     constexpr int kPVUnroll = COMPACT ? 4 : kRows;      // rows of a V tile
     constexpr int kIssueUnroll = COMPACT ? 4 : 8;
     constexpr int NT = kAttnWarps * 32;
