@@ -19,14 +19,19 @@
 // k/v, stored into its T0 slot from the ring), so the next tile -- possibly
 // of the next item -- is in flight while the current one is computed.  The
 // only waits are cp.async.wait_group and CTA barriers; there are no spin loops.
-//   K tile:  lane = row; z_h = q'_h . k for the G query heads of the group,
-//            q' = q * log2(e)/sqrt(d) in shared memory (broadcast reads),
-//            packed f32x2 FMAs; T2 rows: z = scale * (q' . code values).
+//   K tile:  tensor cores (mma.m16n8k16, bf16 operands, fp32 accumulators):
+//            S^T = K q^T for the tile's 32 rows and the group's query heads,
+//            K from the ring by ldmatrix, q^T in registers; z = S^T *
+//            log2(e)/sqrt(d) (times the record's scale for a T2 row, whose
+//            E4M3 codes are first widened in place to bf16, exactly).
 //   stats:   per warp and group, online over its tiles: m_h = max z,
 //            p = 2^(z - m_h), l_h = sum p; z goes to a global scratch for the
 //            alpha sums.
-//   V tile:  the warp walks the tile's rows, lane = 4 (or 2) columns,
-//            O_h += p * v.
+//   V tile:  O^T += V^T p^T on the tensor cores, V^T by a transposing
+//            ldmatrix, p^T from the score fragment by movmatrix; p enters as
+//            two bf16 parts p = hi + lo (about 16 significant bits), each with
+//            its own product into the same fp32 accumulators.  Absent rows of
+//            a partial tile are zero-filled by the copy.
 //   group end: the four warps' (m, l, O) are merged in shared memory (fixed
 //            order) into the CTA's partial for the group, stored at (group,
 //            the CTA's rank among the CTAs that touch the group).
@@ -37,7 +42,7 @@
 // retained counts, never on which tier a row sits in, so a row read from T0 or
 // from T1 staging gives bit-identical results.  No atomics touch `out` or `g`.
 // Launches in which every warp streams at most two tiles use a compact
-// instantiation (partly unrolled loops, same arithmetic in the same order).
+// instantiation (partly unrolled issue loops, same arithmetic in the same order).
 #include <algorithm>
 #include <cmath>
 
@@ -46,32 +51,33 @@
 namespace tkv {
 
 constexpr int kAttnWarps = 4;
-constexpr int kWarpStages = 2;
+constexpr int kTileRows = 16;             // rows per pipeline tile (one m16 block of the products)
+constexpr int kWarpStages = 4;            // tiles per warp ring: three in flight while one is used
+constexpr int kCompactRows = 256;         // CTA windows up to this many rows use the compact instantiation
+constexpr int kMinItemRows = 128;         // item sizes: 128 or 256 rows
 constexpr int kMaxWindowRows = 3584;       // retained-list rows a CTA stages in shared memory
                                            // (two CTAs of the largest instantiation fit an SM)
-constexpr int kCombineRows = 256;          // alpha rows per combine block (one per thread)
+constexpr int kCombineThreads = 256;       // combine block size (one out element per thread)
+constexpr int kCombineRowsPerThread = 4;   // alpha rows per combine thread
+constexpr int kCombineRows = kCombineThreads * kCombineRowsPerThread;
 
 template <int G, int D>
 struct AttnCfg {
-    static constexpr int GP = (G <= 4) ? 4 : 8;      // z / p row stride (floats)
-    static constexpr int ROWB = 2 * D + 16;          // ring row stride (bytes), bank-skewed
-    static constexpr int CPL = D / 32;               // V columns per lane
+    static constexpr int GP = (G <= 4) ? 4 : 8;      // z row stride (floats)
+    static constexpr int ROWB = 2 * D + 16;          // ring row stride (bytes): 8 consecutive rows
+                                                     // hit 8 different 16-byte bank groups
     static_assert(D == 64 || D == 128, "head_dim must be 64 or 128");
     static_assert(G >= 1 && G <= 8, "group size must be 1..8");
 
-    static constexpr size_t sz_stage = (size_t)kRows * ROWB;
+    static constexpr size_t sz_stage = (size_t)kTileRows * ROWB;
     static constexpr size_t sz_warp_ring = kWarpStages * sz_stage;
     static constexpr int PS = 16 + G * D;            // floats of one (m[8], l[8], O[G][D]) record
     static constexpr size_t off_ring = 0;
-    static constexpr size_t off_q = kAttnWarps * sz_warp_ring;
-    // p as (p, p) pairs, one row of PSTR floats per tile row: PSTR * 4 bytes is an odd multiple
-    // of 16, so the lanes that write different rows hit different banks
-    static constexpr int PSTR = 2 * GP + 4;
-    static constexpr size_t off_p = off_q + (size_t)G * D * 4;
-    static constexpr size_t off_comb = off_p + (size_t)kAttnWarps * kRows * PSTR * 4;
+    static constexpr size_t off_comb = kAttnWarps * sz_warp_ring;
     static constexpr size_t off_n = off_comb + (size_t)kAttnWarps * PS * 4;   // rows of each item
     // per item: rows, decode-token flag, (sequence << 16 | KV head)
-    static constexpr size_t off_rl = off_n + (size_t)(kMaxWindowRows / 128) * 3 * 4;
+    static constexpr size_t off_mask = off_n + (size_t)(kMaxWindowRows / kMinItemRows) * 3 * 4;   // T2 rows per ring slot
+    static constexpr size_t off_rl = off_mask + (size_t)kAttnWarps * kWarpStages * 4;
 
     static size_t smem(int rl_rows) { return off_rl + (size_t)rl_rows * 4; }
 };
@@ -83,30 +89,86 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_prev() {
     asm volatile("cp.async.wait_group %0;" ::"n"(kWarpStages - 1) : "memory");
 }
+// 4 bytes global -> shared
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+// 16 zero bytes into shared memory (a source size of 0: nothing is read from `src`)
+__device__ __forceinline__ void cp_async16_zero(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(0) : "memory");
+}
+// four 8 x 8 bf16 matrices from shared memory (lanes 8i..8i+7 address the rows of matrix i)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+// the same, each matrix transposed on the way
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+// transpose of an 8 x 8 bf16 matrix held one (row, column pair) per lane
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+// c += A (16 x 16, bf16) * B (16 x 8, bf16), fp32 accumulators
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Widens the T2 record at `row` (D E4M3 codes, then the fp32 scale) in place to a row of
+// D bf16 values (every E4M3 value is exact in bf16); returns the scale.
+template <int D>
+__device__ __forceinline__ float widen_t2_row(uint8_t* row) {
+    const float sc = *reinterpret_cast<const float*>(row + D);
+    uint4 codes[D / 16];
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) codes[c] = reinterpret_cast<const uint4*>(row)[c];
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+        const uint32_t w[4] = {codes[c].x, codes[c].y, codes[c].z, codes[c].w};
+        uint32_t outw[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 lo = e4m3x2_to_float2((uint16_t)(w[i] & 0xFFFF));
+            const float2 hi = e4m3x2_to_float2((uint16_t)(w[i] >> 16));
+            const __nv_bfloat162 blo = __floats2bfloat162_rn(lo.x, lo.y);
+            const __nv_bfloat162 bhi = __floats2bfloat162_rn(hi.x, hi.y);
+            outw[2 * i] = *reinterpret_cast<const uint32_t*>(&blo);
+            outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bhi);
+        }
+        reinterpret_cast<uint4*>(row)[2 * c] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        reinterpret_cast<uint4*>(row)[2 * c + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+    }
+    return sc;
+}
 
-// COMPACT: partly unrolled loops, for launches in which every warp streams one or two
-// tiles: the code then runs about once per launch and the instruction cache, not the
+// COMPACT: partly unrolled issue loops, for launches in which every warp streams one or
+// two tiles: the code then runs about once per launch and the instruction cache, not the
 // arithmetic, sets its pace.
 template <int G, int D, bool COMPACT>
 __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
-    constexpr int GP = C::GP, ROWB = C::ROWB, CPL = C::CPL, PS = C::PS, PSTR = C::PSTR;
-    // QK lane map: a lane takes rows (lane & 15) and (lane & 15) + 16 of a tile and the query
-    // heads of its half-warp: heads [0, GH) for lanes 0-15, [GH, G) for lanes 16-31.  Each q
-    // element read from shared memory then feeds two rows.
-    constexpr int GH = (G + 1) / 2;
-    constexpr int kQKUnroll = COMPACT ? 4 : 8;          // chunks of 8 elements of a K row (half a row:
-                                                        // a smaller loop body, fewer instruction-cache misses)
-    constexpr int kPVUnroll = COMPACT ? 4 : kRows;      // rows of a V tile
+    constexpr int GP = C::GP, ROWB = C::ROWB, PS = C::PS;
     constexpr int kIssueUnroll = COMPACT ? 4 : 8;
+    constexpr int MT = kTileRows / 16;                  // 16-row blocks of a tile
     constexpr int NT = kAttnWarps * 32;
     extern __shared__ __align__(128) uint8_t smem[];
-    float* q_s = reinterpret_cast<float*>(smem + C::off_q);
     float* comb = reinterpret_cast<float*>(smem + C::off_comb);
     uint32_t* rl_s = reinterpret_cast<uint32_t*>(smem + C::off_rl);
     int* n_s = reinterpret_cast<int*>(smem + C::off_n);
-    int* own_s = n_s + kMaxWindowRows / 128;
-    int* bk_s = n_s + 2 * (kMaxWindowRows / 128);
+    int* own_s = n_s + kMaxWindowRows / kMinItemRows;
+    int* bk_s = n_s + 2 * (kMaxWindowRows / kMinItemRows);
 
     // the combine kernel may be scheduled once every CTA of this grid has started
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -117,11 +179,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     const int it1 = min(total_items, it0 + a.items_per_cta);
     if (it0 >= it1) return;
     uint8_t* ring = smem + C::off_ring + (size_t)warp * C::sz_warp_ring;
-    float* p_s = reinterpret_cast<float*>(smem + C::off_p) + (size_t)warp * kRows * C::PSTR;
 
-    // Prologue in one round trip: the rows of every item, the retained-list slices
-    // (read up to the item size, clamped to the capacity; entries past the count
-    // are never used) and the first group's q.
+    // Prologue in one round trip: the rows of every item, and the retained-list slices copied
+    // straight into shared memory by 4-byte cp.async, all in flight at once (read up to the
+    // item size, clamped to the capacity; entries past the count are never used).
     for (int item = it0 + tid; item < it1; item += NT) {
         const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
         const int R = a.rl_count[b];
@@ -130,43 +191,25 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         own_s[item - it0] = (a.new_k != nullptr && R - 1 >= j0 && R - 1 < j0 + IT) ? 1 : 0;
         bk_s[item - it0] = (b << 16) | (g % a.Hkv);
     }
-    for (int item = it0; item < it1; ++item) {
-        const int g = item / IPG, b = g / a.Hkv, j0 = (item % IPG) * IT;
-        const int cap = min(IT, a.Nmax - j0);
-        const uint32_t* src = a.rl_loc + (size_t)b * a.Nmax + j0;
-        uint32_t* dst = rl_s + (size_t)(item - it0) * IT;
-        for (int r = tid; r < cap; r += NT) dst[r] = src[r];
+    for (int i = tid; i < (it1 - it0) * IT; i += NT) {
+        const int item = it0 + i / IT, j = (item % IPG) * IT + i % IT;
+        const int b = item / IPG / a.Hkv;
+        if (j < a.Nmax) cp_async4(smem_u32(rl_s + i), a.rl_loc + (size_t)b * a.Nmax + j);
     }
-    // q of group g, scaled, into shared memory: 8 elements per 16-byte load when q is aligned
-    auto load_q = [&](int g) {
-        const int b = g / a.Hkv, kvh = g % a.Hkv;
-        const __nv_bfloat16* qg = a.q + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
-        if ((reinterpret_cast<uintptr_t>(qg) & 15u) == 0) {
-            for (int i = tid; i < G * D / 8; i += NT) {
-                const uint4 w = reinterpret_cast<const uint4*>(qg)[i];
-                const float2 f0 = bf16x2_to_float2(w.x), f1 = bf16x2_to_float2(w.y);
-                const float2 f2 = bf16x2_to_float2(w.z), f3 = bf16x2_to_float2(w.w);
-                float4* dst = reinterpret_cast<float4*>(q_s + 8 * i);
-                dst[0] = make_float4(f0.x * a.qscale, f0.y * a.qscale, f1.x * a.qscale, f1.y * a.qscale);
-                dst[1] = make_float4(f2.x * a.qscale, f2.y * a.qscale, f3.x * a.qscale, f3.y * a.qscale);
-            }
-        } else {
-            for (int i = tid; i < G * D; i += NT) q_s[i] = __bfloat162float(qg[i]) * a.qscale;
-        }
-    };
-    load_q(it0 / IPG);
+    cp_async_commit();
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    // tiles of this warp in an item: warp, warp + 4, ... below ceil(n / 32)
+    // tiles of this warp in an item: warp, warp + 4, ... below ceil(n / kTileRows)
     auto warp_tiles = [&](int n) {
-        const int nt = (n + kRows - 1) / kRows;
+        const int nt = (n + kTileRows - 1) / kTileRows;
         return warp < nt ? (nt - warp + kAttnWarps - 1) / kAttnWarps : 0;
     };
 
     // row (within tile `tile` of item) of the group's decode token, or -1
     auto new_row_in = [&](int item, int tile) {
         const int n = n_s[item - it0];
-        const int r = n - 1 - tile * kRows;
-        return (own_s[item - it0] && r >= 0 && r < kRows) ? r : -1;
+        const int r = n - 1 - tile * kTileRows;
+        return (own_s[item - it0] && r >= 0 && r < kTileRows) ? r : -1;
     };
 
     // ------------------------------------------------------------ issue side
@@ -180,8 +223,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
     const uint8_t* stg = reinterpret_cast<const uint8_t*>(a.stage);
     const uint8_t* row_v = nullptr;    // the lane's V row of the tile whose K was issued last
     int row_bytes = 0;
-    uint32_t fp8_mask_issue = 0;       // T2 rows of the tile last issued as K
-    bool all_bf16_issue = false;       // that tile has 32 bf16 rows (its K and V copies take the fast path)
+    bool all_bf16_issue = false;       // the tile last issued as K has kTileRows bf16 rows (its K and V
+                                       // copies take the fast path)
+    uint32_t* mask_s = reinterpret_cast<uint32_t*>(smem + C::off_mask) + warp * kWarpStages;
     // Copies the next tile of this warp's sequence: 16 lanes per 256-byte row, 16 bytes
     // a lane; a row's source pointer travels by shuffle with its kind in the low bits
     // (bit 0: T2 record of D + 16 bytes, bit 1: no row).
@@ -190,13 +234,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         const int item = ci_item, kv = ci_kv;
         const int n = n_s[item - it0];
         const int tile = warp + kAttnWarps * ci_k;
-        const int jl = tile * kRows + lane;
+        const int jl = tile * kTileRows + lane;
         const uint8_t* src = nullptr;
         if (kv == 0) {
             const int bk = bk_s[item - it0], b = bk >> 16, kvh = bk & 0xFFFF;
             row_bytes = 0;
             bool fp8 = false;
-            if (jl < n) {
+            if (lane < kTileRows && jl < n) {
                 const uint32_t loc = rl_s[(size_t)(item - it0) * IT + jl];
                 const int tier = loc_tier(loc), slot = loc_slot(loc);
                 if (tier == 0) {
@@ -219,17 +263,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                     row_v = reinterpret_cast<const uint8_t*>(a.new_v + ((size_t)b * a.Hkv + kvh) * D);
                 }
             }
-            fp8_mask_issue = __ballot_sync(0xffffffffu, fp8);
+            // the T2 rows of this K tile, for the consumer of its slot (and of the V slot after it)
+            const uint32_t fm = __ballot_sync(0xffffffffu, fp8);
+            if (lane == 0) mask_s[issued % kWarpStages] = fm;
         } else {
             src = row_v;
         }
-        if (kv == 0) all_bf16_issue = __all_sync(0xffffffffu, row_bytes == 2 * D);
+        if (kv == 0) all_bf16_issue = __all_sync(0xffffffffu, lane >= kTileRows || row_bytes == 2 * D);
         const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * C::sz_stage);
         const int col = lane & 15, half = lane >> 4;
         if (all_bf16_issue) {
-            // 32 bf16 rows: no per-row kinds to decode
+            // kTileRows bf16 rows: no per-row kinds to decode
 #pragma unroll kIssueUnroll
-            for (int rr = 0; rr < kRows / 2; ++rr) {
+            for (int rr = 0; rr < kTileRows / 2; ++rr) {
                 const int r = 2 * rr + half;
                 const uint8_t* rsrc = reinterpret_cast<const uint8_t*>(
                     __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), r));
@@ -239,12 +285,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
             const unsigned long long tagged = (unsigned long long)src | (row_bytes == D + 16 ? 1ull : 0ull) |
                                               (row_bytes ? 0ull : 2ull);
 #pragma unroll 4
-            for (int rr = 0; rr < kRows / 2; ++rr) {
+            for (int rr = 0; rr < kTileRows / 2; ++rr) {
                 const int r = 2 * rr + half;
                 const unsigned long long t = __shfl_sync(0xffffffffu, tagged, r);
                 const uint8_t* rsrc = (const uint8_t*)(t & ~15ull);
                 const int nb = (t & 2ull) ? 0 : ((t & 1ull) ? D + 16 : 2 * D);
-                if (col * 16 < nb) cp_async16(dst0 + r * ROWB + col * 16, rsrc + col * 16);
+                if (col * 16 < nb)
+                    cp_async16(dst0 + r * ROWB + col * 16, rsrc + col * 16);
+                else if (nb == 0 && col * 16 < 2 * D)
+                    cp_async16_zero(dst0 + r * ROWB + col * 16, k0v0);   // absent row: zeros, so that
+                                                                         // p = 0 meets no NaN in the product
             }
         }
         ++issued;
@@ -260,48 +310,78 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         }
     };
 
-    issue_next();
-    cp_async_commit();
+    // the first kWarpStages - 1 copies (empty groups past the end of the sequence)
+#pragma unroll
+    for (int i = 0; i < kWarpStages - 1; ++i) {
+        issue_next();
+        cp_async_commit();
+    }
     int consumed = 0;
 
     // ---------------------------------------------------- per-warp segment state
-    const int rp = lane & 15, hg = lane >> 4;
-    const int hbase = hg * GH;                       // first head of this lane's half-warp
-    const int nh = hg ? G - GH : GH;                 // heads of this lane's half-warp
-    float m_w[G], l_g[GH];                           // running max (all heads); sum of p (own heads)
-    float2 o[G][CPL / 2];
-    auto reset_segment = [&]() {
+    // Tensor-core fragments (mma.m16n8k16, bf16 in, fp32 accumulate).  A lane holds, of a
+    // 16 x 8 accumulator, rows gq and gq + 8 and columns 2 cq, 2 cq + 1:
+    //   scores  S^T[row][head] = k_row . q_head  (A: K rows from the ring, B: q^T);
+    //   output  O^T[d][head]  += v_row[d] * p    (A: V^T from the ring, B: p^T).
+    // Both put this lane's values on the query heads h0 = 2 cq and h1 = 2 cq + 1, so the
+    // softmax rescale of O needs no exchange.  Heads past G are zero columns of q^T.
+    const int gq = lane >> 2, cq = lane & 3;
+    const int h0 = 2 * cq, h1 = 2 * cq + 1;
+    uint32_t qf[D / 16][2];                          // q^T B fragments of the current group
+    float m_r[2], l_r[2];                            // running max (warp-uniform) and this lane's share of l
+    float o[D / 16][4];
+    auto load_q = [&](int g) {
+        const int b = g / a.Hkv, kvh = g % a.Hkv;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            m_w[h] = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < CPL / 2; ++c) o[h][c] = make_float2(0.f, 0.f);
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t lo = 0u, hi = 0u;
+            if (gq < G) {
+                const unsigned short* qh = reinterpret_cast<const unsigned short*>(
+                    a.q + ((size_t)b * a.Hq + (size_t)kvh * G + gq) * D + ks * 16 + 2 * cq);
+                lo = (uint32_t)qh[0] | ((uint32_t)qh[1] << 16);
+                hi = (uint32_t)qh[8] | ((uint32_t)qh[9] << 16);
+            }
+            qf[ks][0] = lo;
+            qf[ks][1] = hi;
         }
+    };
+    auto reset_segment = [&]() {
+        m_r[0] = m_r[1] = -INFINITY;
+        l_r[0] = l_r[1] = 0.f;
 #pragma unroll
-        for (int h = 0; h < GH; ++h) l_g[h] = 0.f;
+        for (int dt = 0; dt < D / 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     };
     // merges the four warps' (m, l, O) of group g into this CTA's partial record for g
     auto flush_segment = [&](int g) {
         float* cw = comb + (size_t)warp * PS;
+        float l0 = l_r[0], l1 = l_r[1];
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
-            // sum over the half-warp that owns head hbase + h
-            float l = l_g[h];
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            if (rp == 0 && h < nh) cw[8 + hbase + h] = l;
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
-        if (lane < G) {
-            float m = m_w[0];
-#pragma unroll
-            for (int h = 1; h < G; ++h) m = lane == h ? m_w[h] : m;
-            cw[lane] = m;
+        if (gq == 0) {
+            if (h0 < G) {
+                cw[h0] = m_r[0];
+                cw[8 + h0] = l0;
+            }
+            if (h1 < G) {
+                cw[h1] = m_r[1];
+                cw[8 + h1] = l1;
+            }
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int c = 0; c < CPL / 2; ++c)
-                *reinterpret_cast<float2*>(cw + 16 + h * D + lane * CPL + 2 * c) = o[h][c];
+        for (int dt = 0; dt < D / 16; ++dt) {
+            const int d = dt * 16 + gq;
+            if (h0 < G) {
+                cw[16 + h0 * D + d] = o[dt][0];
+                cw[16 + h0 * D + d + 8] = o[dt][2];
+            }
+            if (h1 < G) {
+                cw[16 + h1 * D + d] = o[dt][1];
+                cw[16 + h1 * D + d + 8] = o[dt][3];
+            }
+        }
         __syncthreads();
         // record (g, this CTA's rank among the CTAs that touch g)
         const int c_lo = (g * IPG) / a.items_per_cta;
@@ -327,6 +407,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         }
         __syncthreads();
     };
+    // ldmatrix lane offsets within a stage: K rows as the A operand (row-major 16 x 16 blocks)
+    // and V rows as the transposed A operand of the output product
+    const uint32_t k_lane = (uint32_t)(((lane & 7) + ((lane >> 3) & 1) * 8) * ROWB + (lane >> 4) * 16);
+    const uint32_t v_lane = (uint32_t)(((lane & 7) + ((lane >> 4) & 1) * 8) * ROWB + ((lane >> 3) & 1) * 16);
 
     int cur_group = -1;
     for (int item = it0; item < it1; ++item) {
@@ -334,11 +418,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         const int j0 = (item % IPG) * IT;
         const int n = n_s[item - it0];
         if (g != cur_group) {
-            if (cur_group >= 0) {
-                flush_segment(cur_group);
-                load_q(g);
-                __syncthreads();
-            }
+            if (cur_group >= 0) flush_segment(cur_group);
+            load_q(g);
             reset_segment();
             cur_group = g;
         }
@@ -346,21 +427,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         float* zg = a.zs + (((size_t)b * a.Hkv + kvh) * a.Nmax + j0) * GP;
         for (int k = 0; k < nt; ++k) {
             const int tile = warp + kAttnWarps * k;
-            const int ra = rp, rb = rp + 16;           // this lane's rows in the tile
-            const int ja = tile * kRows + ra, jb = tile * kRows + rb;
-            const bool valid_a = ja < n, valid_b = jb < n;
+            const int nrows = min(kTileRows, n - tile * kTileRows);
 
             // ---------------------------------------------------------- K tile
             issue_next();                       // the V tile of this tile
             cp_async_commit();
-            const uint32_t tmask = fp8_mask_issue;
             cp_async_wait_prev();
             __syncwarp();
+            const uint32_t tmask = mask_s[consumed % kWarpStages];
             // the decode token's rows go from the ring into their T0 slot (K now, V below)
             const int newr = new_row_in(item, tile);
             auto store_new_row = [&](int kv) {
                 if (lane < 2 * D / 16) {
-                    const int slot = loc_slot(rl_s[(size_t)(item - it0) * IT + tile * kRows + newr]);
+                    const int slot = loc_slot(rl_s[(size_t)(item - it0) * IT + tile * kTileRows + newr]);
                     const uint8_t* srow = ring + (size_t)(consumed % kWarpStages) * C::sz_stage + (size_t)newr * ROWB;
                     uint8_t* drow = reinterpret_cast<uint8_t*>(const_cast<__nv_bfloat16*>(a.k0v0)) +
                                     row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S0) * (2 * D);
@@ -368,154 +447,111 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
                 }
             };
             if (newr >= 0) store_new_row(0);
-            float za[GH], zb[GH];
+            uint8_t* stage_k = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
+            // row scales of this lane's score rows (tile rows gq + 8 i): log2(e)/sqrt(d), times
+            // the record's scale for a T2 row
+            float rs[2 * MT];
+#pragma unroll
+            for (int i = 0; i < 2 * MT; ++i) rs[i] = a.qscale;
+            if (tmask != 0u) {
+                // every T2 record of the stage is widened in place to a bf16 row (E4M3 values are
+                // exact in bf16), row r by lane r; the scale of row r stays with lane r
+                const float my_sc = ((tmask >> lane) & 1u) ? widen_t2_row<D>(stage_k + (size_t)lane * ROWB) : 1.0f;
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 2 * MT; ++i) rs[i] *= __shfl_sync(0xffffffffu, my_sc, gq + 8 * i);
+            }
+            // two accumulator chains (even and odd 16-column steps of d), added at the end
+            float s[MT][4], s2[MT][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s[mt][i] = s2[mt][i] = 0.f;
             {
-                const uint8_t* stage_k = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
-                const uint8_t* row_a = stage_k + (size_t)ra * ROWB;
-                const uint8_t* row_b = stage_k + (size_t)rb * ROWB;
-                // two independent accumulator pairs per (row, head): (k0, k2) and (k1, k3) of each chunk
-                float2 acca[GH], acca2[GH], accb[GH], accb2[GH];
+                const uint32_t kb = smem_u32(stage_k) + k_lane;
 #pragma unroll
-                for (int h = 0; h < GH; ++h) acca[h] = acca2[h] = accb[h] = accb2[h] = make_float2(0.f, 0.f);
-                // eight elements of a row from its chunk c: bf16, or E4M3 codes of a T2 record
-                auto load8 = [&](const uint8_t* row, bool f8, int c, float2& k0, float2& k1, float2& k2, float2& k3) {
-                    if (!f8) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
-                        k0 = bf16x2_to_float2(w.x);
-                        k1 = bf16x2_to_float2(w.y);
-                        k2 = bf16x2_to_float2(w.z);
-                        k3 = bf16x2_to_float2(w.w);
-                    } else {
-                        const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
-                        k0 = e4m3x2_to_float2((uint16_t)(w.x & 0xFFFF));
-                        k1 = e4m3x2_to_float2((uint16_t)(w.x >> 16));
-                        k2 = e4m3x2_to_float2((uint16_t)(w.y & 0xFFFF));
-                        k3 = e4m3x2_to_float2((uint16_t)(w.y >> 16));
+                for (int ks = 0; ks < D / 16; ks += 2)
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+                        ldsm_x4(kb + (uint32_t)(mt * 16 * ROWB + ks * 32), a0, a1, a2, a3);
+                        ldsm_x4(kb + (uint32_t)(mt * 16 * ROWB + ks * 32 + 32), c0, c1, c2, c3);
+                        mma_bf16(s[mt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                        mma_bf16(s2[mt], c0, c1, c2, c3, qf[ks + 1][0], qf[ks + 1][1]);
                     }
-                };
-                auto qk_chunk = [&](int c, bool fa, bool fb) {
-                    float2 a0, a1, a2, a3, b0, b1, b2, b3;
-                    load8(row_a, fa, c, a0, a1, a2, a3);
-                    load8(row_b, fb, c, b0, b1, b2, b3);
 #pragma unroll
-                    for (int h = 0; h < GH; ++h) {
-                        // heads past G (the short half-warp of an odd G) read head G - 1; discarded
-                        const float* qh = q_s + (size_t)min(hbase + h, G - 1) * D + c * 8;
-                        const float4 qa = *reinterpret_cast<const float4*>(qh);
-                        const float4 qb = *reinterpret_cast<const float4*>(qh + 4);
-                        acca[h] = __ffma2_rn(make_float2(qa.x, qa.y), a0, acca[h]);
-                        accb[h] = __ffma2_rn(make_float2(qa.x, qa.y), b0, accb[h]);
-                        acca2[h] = __ffma2_rn(make_float2(qa.z, qa.w), a1, acca2[h]);
-                        accb2[h] = __ffma2_rn(make_float2(qa.z, qa.w), b1, accb2[h]);
-                        acca[h] = __ffma2_rn(make_float2(qb.x, qb.y), a2, acca[h]);
-                        accb[h] = __ffma2_rn(make_float2(qb.x, qb.y), b2, accb[h]);
-                        acca2[h] = __ffma2_rn(make_float2(qb.z, qb.w), a3, acca2[h]);
-                        accb2[h] = __ffma2_rn(make_float2(qb.z, qb.w), b3, accb2[h]);
-                    }
-                };
-                float sca = 1.0f, scb = 1.0f;
-                if (tmask != 0u) {
-                    // A tile with T2 rows: every T2 record of the stage is widened in place to a
-                    // bf16 row (E4M3 values are exact in bf16), one row per lane -- row ra by
-                    // the lanes 0-15, row rb by the lanes 16-31 -- and its scale kept aside; the
-                    // dot products then run the bf16 loop and are scaled after it.
-                    uint8_t* mine = const_cast<uint8_t*>(hg ? row_b : row_a);
-                    float my_sc = 1.0f;
-                    if ((tmask >> (hg ? rb : ra)) & 1u) {
-                        my_sc = *reinterpret_cast<const float*>(mine + D);
-                        uint4 codes[D / 16];
+                for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int c = 0; c < D / 16; ++c) codes[c] = reinterpret_cast<const uint4*>(mine)[c];
-#pragma unroll
-                        for (int c = 0; c < D / 16; ++c) {
-                            const uint32_t w[4] = {codes[c].x, codes[c].y, codes[c].z, codes[c].w};
-                            uint32_t outw[8];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 lo = e4m3x2_to_float2((uint16_t)(w[i] & 0xFFFF));
-                                const float2 hi = e4m3x2_to_float2((uint16_t)(w[i] >> 16));
-                                const __nv_bfloat162 blo = __floats2bfloat162_rn(lo.x, lo.y);
-                                const __nv_bfloat162 bhi = __floats2bfloat162_rn(hi.x, hi.y);
-                                outw[2 * i] = *reinterpret_cast<const uint32_t*>(&blo);
-                                outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bhi);
-                            }
-                            reinterpret_cast<uint4*>(mine)[2 * c] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-                            reinterpret_cast<uint4*>(mine)[2 * c + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-                        }
-                    }
-                    __syncwarp();
-                    // the scale of row ra sits with lane ra, that of row rb with lane 16 + rb - 16
-                    sca = __shfl_sync(0xffffffffu, my_sc, rp);
-                    scb = __shfl_sync(0xffffffffu, my_sc, 16 + rp);
-                }
-#pragma unroll kQKUnroll
-                for (int c = 0; c < D / 8; ++c) qk_chunk(c, false, false);
-#pragma unroll
-                for (int h = 0; h < GH; ++h) {
-                    const bool live = h < nh;
-                    za[h] = (valid_a && live) ? ((acca[h].x + acca[h].y) + (acca2[h].x + acca2[h].y)) * sca : -INFINITY;
-                    zb[h] = (valid_b && live) ? ((accb[h].x + accb[h].y) + (accb2[h].x + accb2[h].y)) * scb : -INFINITY;
-                }
+                    for (int i = 0; i < 4; ++i) s[mt][i] += s2[mt][i];
             }
             __syncwarp();
             ++consumed;
 
             // ------------------------------ online softmax update (warp-uniform max)
-            // tile maxima of this half-warp's heads, then the other half-warp's by one exchange
-            float tmax[G];
+            // z[mt][i]: tile row mt * 16 + gq + 8 (i >> 1), head h0 + (i & 1); absent rows and
+            // heads past G are -inf
+            float z[MT][4];
 #pragma unroll
-            for (int h = 0; h < GH; ++h) {
-                float tm = fmaxf(za[h], zb[h]);
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                for (int off = 8; off > 0; off >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, off));
-                const float other = __shfl_xor_sync(0xffffffffu, tm, 16);
-                tmax[h] = hg ? other : tm;
-                if (GH + h < G) tmax[GH + h] = hg ? tm : other;
+                for (int i = 0; i < 4; ++i) {
+                    const int r = mt * 16 + gq + 8 * (i >> 1);
+                    const bool live = r < nrows && h0 + (i & 1) < G;
+                    z[mt][i] = live ? s[mt][i] * rs[2 * mt + (i >> 1)] : -INFINITY;
+                }
+            float tm0 = fmaxf(z[0][0], z[0][2]), tm1 = fmaxf(z[0][1], z[0][3]);
+#pragma unroll
+            for (int mt = 1; mt < MT; ++mt) {
+                tm0 = fmaxf(tm0, fmaxf(z[mt][0], z[mt][2]));
+                tm1 = fmaxf(tm1, fmaxf(z[mt][1], z[mt][3]));
             }
-            float sc_all[G];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float m_new = fmaxf(m_w[h], tmax[h]);
-                sc_all[h] = (m_w[h] == -INFINITY) ? 0.f : exp2f(m_w[h] - m_new);
-                m_w[h] = m_new;
-#pragma unroll
-                for (int c = 0; c < CPL / 2; ++c) o[h][c] = __fmul2_rn(o[h][c], make_float2(sc_all[h], sc_all[h]));
+            for (int off = 4; off < 32; off <<= 1) {
+                tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, off));
+                tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, off));
             }
-            float pa[GH], pb[GH];
+            const float mn0 = fmaxf(m_r[0], tm0), mn1 = fmaxf(m_r[1], tm1);
+            const float sc0 = (m_r[0] == -INFINITY) ? 0.f : exp2f(m_r[0] - mn0);
+            const float sc1 = (m_r[1] == -INFINITY) ? 0.f : exp2f(m_r[1] - mn1);
+            m_r[0] = mn0;
+            m_r[1] = mn1;
+            // an unchanged maximum gives a factor of exactly 1: O is rescaled only when some
+            // head's maximum moved
+            if (__any_sync(0xffffffffu, sc0 != 1.f || sc1 != 1.f)) {
 #pragma unroll
-            for (int h = 0; h < GH; ++h) {
-                // this lane's head hbase + h: its scale and new max, selected without indexing
-                const float sc = (hg && GH + h < G) ? sc_all[GH + h < G ? GH + h : 0] : sc_all[h];
-                const float mh = (hg && GH + h < G) ? m_w[GH + h < G ? GH + h : 0] : m_w[h];
-                l_g[h] *= sc;
-                pa[h] = za[h] == -INFINITY ? 0.f : exp2f(za[h] - mh);
-                pb[h] = zb[h] == -INFINITY ? 0.f : exp2f(zb[h] - mh);
-                l_g[h] += pa[h];
-                l_g[h] += pb[h];
-            }
-            // p as (p, p) pairs of this lane's heads, rows ra and rb
-#pragma unroll
-            for (int h = 0; h < GH; ++h) {
-                if (h < nh) {
-                    *reinterpret_cast<float2*>(p_s + (size_t)ra * PSTR + 2 * (hbase + h)) = make_float2(pa[h], pa[h]);
-                    *reinterpret_cast<float2*>(p_s + (size_t)rb * PSTR + 2 * (hbase + h)) = make_float2(pb[h], pb[h]);
+                for (int dt = 0; dt < D / 16; ++dt) {
+                    o[dt][0] *= sc0;
+                    o[dt][1] *= sc1;
+                    o[dt][2] *= sc0;
+                    o[dt][3] *= sc1;
                 }
             }
+            float p[MT][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    p[mt][i] = z[mt][i] == -INFINITY ? 0.f : exp2f(z[mt][i] - ((i & 1) ? mn1 : mn0));
+            float ps0 = p[0][0] + p[0][2], ps1 = p[0][1] + p[0][3];
+#pragma unroll
+            for (int mt = 1; mt < MT; ++mt) {
+                ps0 += p[mt][0] + p[mt][2];
+                ps1 += p[mt][1] + p[mt][3];
+            }
+            l_r[0] = l_r[0] * sc0 + ps0;
+            l_r[1] = l_r[1] * sc1 + ps1;
             // logits of this lane's heads for the alpha sums (slots of heads past G are never read)
-            auto store_z = [&](float* dst, const float* z) {
-                if constexpr (GH == 4) {
-                    *reinterpret_cast<float4*>(dst) = make_float4(z[0], z[1], z[2], z[3]);
-                } else if constexpr (GH == 2) {
-                    *reinterpret_cast<float2*>(dst) = make_float2(z[0], z[1]);
-                } else {
+            if (h0 < GP) {
 #pragma unroll
-                    for (int h = 0; h < GH; ++h)
-                        if (h < nh) dst[h] = z[h];
-                }
-            };
-            if (valid_a) store_z(zg + (size_t)ja * GP + hbase, za);
-            if (valid_b) store_z(zg + (size_t)jb * GP + hbase, zb);
-            __syncwarp();
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int r = mt * 16 + gq + 8 * hh;
+                        if (r < nrows)
+                            *reinterpret_cast<float2*>(zg + (size_t)(tile * kTileRows + r) * GP + h0) =
+                                make_float2(z[mt][2 * hh], z[mt][2 * hh + 1]);
+                    }
+            }
 
             // ---------------------------------------------------------- V tile
             issue_next();                       // the next K tile
@@ -524,50 +560,43 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
             __syncwarp();
             if (newr >= 0) store_new_row(1);
             {
-                const int nrows = min(kRows, n - tile * kRows);
-                const uint8_t* stage = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
-                // o[h] += p[h] * v for one row; p read as (p, p) pairs
-                auto pv_row = [&](int r, bool fp8) {
-                    const uint8_t* row = stage + (size_t)r * ROWB;
-                    float2 pp[G];
+                uint8_t* stage_v = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
+                if (tmask != 0u) {
+                    // T2 rows: widened in place as on the K side; p of such a row carries its scale
+                    const float my_sc = ((tmask >> lane) & 1u) ? widen_t2_row<D>(stage_v + (size_t)lane * ROWB) : 1.0f;
+                    __syncwarp();
 #pragma unroll
-                    for (int h = 0; h < G; h += 2) {
-                        const float4 t = *reinterpret_cast<const float4*>(p_s + (size_t)r * PSTR + 2 * h);
-                        pp[h] = make_float2(t.x, t.y);
-                        if (h + 1 < G) pp[h + 1] = make_float2(t.z, t.w);
-                    }
-                    float2 v[CPL / 2];
-                    if (!fp8) {
-                        if (CPL == 4) {
-                            const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
-                            v[0] = bf16x2_to_float2(w.x);
-                            v[CPL / 2 - 1] = bf16x2_to_float2(w.y);
-                        } else {
-                            v[0] = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(row + lane * 4));
-                        }
-                    } else {
-                        const float sc = *reinterpret_cast<const float*>(row + D);
+                    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int h = 0; h < G; ++h) pp[h] = __fmul2_rn(pp[h], make_float2(sc, sc));
-                        if (CPL == 4) {
-                            const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
-                            v[0] = e4m3x2_to_float2((uint16_t)(w & 0xFFFF));
-                            v[CPL / 2 - 1] = e4m3x2_to_float2((uint16_t)(w >> 16));
-                        } else {
-                            v[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(row + lane * 2));
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const float vs = __shfl_sync(0xffffffffu, my_sc, mt * 16 + gq + 8 * hh);
+                            p[mt][2 * hh] *= vs;
+                            p[mt][2 * hh + 1] *= vs;
                         }
+                }
+                const uint32_t vb = smem_u32(stage_v) + v_lane;
+#pragma unroll
+                for (int kk = 0; kk < MT; ++kk) {
+                    // p^T as B operands, split p = hi + lo into two bf16 parts (about 16
+                    // significant bits together); rows gq and gq + 8 of this 16-row step
+                    uint32_t bh[2], bl[2];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const float x = p[kk][2 * hh], y = p[kk][2 * hh + 1];
+                        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(x, y);
+                        const uint32_t hw = *reinterpret_cast<const uint32_t*>(&hi2);
+                        const float2 hf = bf16x2_to_float2(hw);
+                        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+                        bh[hh] = movmatrix_t(hw);
+                        bl[hh] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&lo2));
                     }
 #pragma unroll
-                    for (int h = 0; h < G; ++h)
-#pragma unroll
-                        for (int c = 0; c < CPL / 2; ++c) o[h][c] = __ffma2_rn(pp[h], v[c], o[h][c]);
-                };
-                if (nrows == kRows && tmask == 0u) {
-#pragma unroll kPVUnroll
-                    for (int r = 0; r < kRows; ++r) pv_row(r, false);
-                } else {
-#pragma unroll 4
-                    for (int r = 0; r < nrows; ++r) pv_row(r, (tmask >> r) & 1u);
+                    for (int dt = 0; dt < D / 16; ++dt) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_t(vb + (uint32_t)(kk * 16 * ROWB + dt * 32), a0, a1, a2, a3);
+                        mma_bf16(o[dt], a0, a1, a2, a3, bh[0], bh[1]);
+                        mma_bf16(o[dt], a0, a1, a2, a3, bl[0], bl[1]);
+                    }
                 }
             }
             __syncwarp();
@@ -620,21 +649,26 @@ __global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) 
 #pragma unroll
         for (int k = 0; k < kSegBatch; ++k) v[k] = (has_out && k < ns) ? rec(k)[16 + idx] : 0.f;
     }
-    const int j = blockIdx.x * kCombineRows + threadIdx.x;
-    const bool has_row = j < a.Nmax;
-    float zz[GP];
-    if (has_row) {
-        const float* zg = a.zs + (((size_t)b * a.Hkv + kvh) * a.Nmax + j) * GP;
-#pragma unroll
-        for (int h = 0; h < GP; h += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(zg + h);
-            zz[h] = t.x; zz[h + 1] = t.y; zz[h + 2] = t.z; zz[h + 3] = t.w;
-        }
-    }
+    // this thread's rows: j0 + k * kCombineThreads, k < kCombineRowsPerThread
+    const int j0 = blockIdx.x * kCombineRows + threadIdx.x;
     const int R = a.rl_count[b];
-    // running sum over layers of this row's alpha (layer 0 starts it)
-    float* gj = a.g + ((size_t)b * a.Hkv + kvh) * a.Nmax + j;
-    const float g_prev = (has_row && a.layer > 0) ? *gj : 0.f;
+    float zz[kCombineRowsPerThread][GP];
+    float g_prev[kCombineRowsPerThread];
+    float* gg = a.g + ((size_t)b * a.Hkv + kvh) * a.Nmax;
+#pragma unroll
+    for (int k = 0; k < kCombineRowsPerThread; ++k) {
+        const int j = j0 + k * kCombineThreads;
+        if (j < R) {
+            const float* zg = a.zs + (((size_t)b * a.Hkv + kvh) * a.Nmax + j) * GP;
+#pragma unroll
+            for (int h = 0; h < GP; h += 4) {
+                const float4 t = *reinterpret_cast<const float4*>(zg + h);
+                zz[k][h] = t.x; zz[k][h + 1] = t.y; zz[k][h + 2] = t.z; zz[k][h + 3] = t.w;
+            }
+        }
+        // running sum over layers of this row's alpha (layer 0 starts it)
+        g_prev[k] = (j < R && a.layer > 0) ? gg[j] : 0.f;
+    }
     __syncthreads();
     // (2) the group's M and L per head (one warp per head, segments across lanes, fixed
     // shuffle order), and every segment's factor 2^(m - M) / L
@@ -681,11 +715,15 @@ __global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) 
         a.out[((size_t)b * a.Hq + (size_t)kvh * G) * D + idx] = acc;
     }
     // (4) alpha sums of this block's rows
-    if (has_row && j < R) {
-        float acc = 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc += exp2f(zz[h] - Ms[h]) * Linv[h];
-        *gj = g_prev + acc;
+    for (int k = 0; k < kCombineRowsPerThread; ++k) {
+        const int j = j0 + k * kCombineThreads;
+        if (j < R) {
+            float acc = 0.f;
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc += exp2f(zz[k][h] - Ms[h]) * Linv[h];
+            gg[j] = g_prev[k] + acc;
+        }
     }
 }
 
@@ -695,7 +733,7 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st, cudaEvent_t aft
     using C = AttnCfg<G, D>;
     const size_t smem = C::smem(a.items_per_cta * a.item_rows);
     // at most two tiles per warp: the compact instantiation
-    if (a.items_per_cta * a.item_rows <= 2 * kRows * kAttnWarps)
+    if (a.items_per_cta * a.item_rows <= kCompactRows)
         attn_kernel<G, D, true><<<a.grid, kAttnWarps * 32, smem, st>>>(a);
     else
         attn_kernel<G, D, false><<<a.grid, kAttnWarps * 32, smem, st>>>(a);
@@ -705,11 +743,11 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st, cudaEvent_t aft
     if (before_combine && (e = cudaEventRecord(before_combine, st)) != cudaSuccess) return e;
     // one alpha row per thread; enough blocks that every block holds at most 256 out elements
     const int rows = a.items_per_group * a.item_rows;
-    const int blocks = std::max((rows + kCombineRows - 1) / kCombineRows, (G * D + kCombineRows - 1) / kCombineRows);
+    const int blocks = std::max((rows + kCombineRows - 1) / kCombineRows, (G * D + kCombineThreads - 1) / kCombineThreads);
     const int max_segs = a.part_per_group;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks, a.B * a.Hkv);
-    cfg.blockDim = dim3(kCombineRows, 1, 1);
+    cfg.blockDim = dim3(kCombineThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)max_segs * 3 * 8 * 4;
     if (cfg.dynamicSmemBytes > 48 * 1024) {
         // raise the limit if needed, never lower it (other contexts may need more)
@@ -733,7 +771,12 @@ template <int G, int D>
 static cudaError_t prepare_gd(size_t smem) {
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<G, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(attn_kernel<G, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(attn_kernel<G, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // the combine kernel asks for the same shared-memory carve-out as the main kernel, so that
+    // an SM need not be reconfigured between the two
+    return cudaFuncSetAttribute(attn_combine_kernel<G, D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared);
 }
 
 template <int G, int D>
@@ -812,24 +855,35 @@ cudaError_t attention_ensure_smem(int G, int d, size_t smem) {
 }
 
 AttnPlan attention_plan(int G, int d, int B, int Hkv, int rmax, int resident) {
-    AttnPlan p{};
     const int groups = B * Hkv;
     rmax = std::max(rmax, 1);
     resident = std::max(resident, 1);
-    // 256-row items, or 128-row items when that is needed to give every resident CTA work
-    p.item_rows = (groups * ((rmax + 255) / 256) >= resident) ? 256 : 128;
-    p.items_per_group = (rmax + p.item_rows - 1) / p.item_rows;
-    const int total = groups * p.items_per_group;
-    p.grid = std::min(total, resident);
-    p.items_per_cta = (total + p.grid - 1) / p.grid;
-    const int max_items = kMaxWindowRows / p.item_rows;
-    if (p.items_per_cta > max_items) {
-        p.items_per_cta = max_items;
-        p.grid = (total + max_items - 1) / max_items;
+    // Items of 256, 128 or 64 rows: the size whose heaviest CTA streams the fewest rows (waves
+    // of resident CTAs times items per CTA times rows), the larger items on a tie.  The choice
+    // depends on rmax only through ceil(rmax / 64).
+    AttnPlan best{};
+    long best_load = -1;
+    for (int rows = 256; rows >= kMinItemRows; rows /= 2) {
+        AttnPlan p{};
+        p.item_rows = rows;
+        p.items_per_group = (rmax + rows - 1) / rows;
+        const int total = groups * p.items_per_group;
+        p.grid = std::min(total, resident);
+        p.items_per_cta = (total + p.grid - 1) / p.grid;
+        const int max_items = kMaxWindowRows / rows;
+        if (p.items_per_cta > max_items) {
+            p.items_per_cta = max_items;
+            p.grid = (total + max_items - 1) / max_items;
+        }
+        const long load = (long)((p.grid + resident - 1) / resident) * p.items_per_cta * rows;
+        if (best_load < 0 || load < best_load) {
+            best = p;
+            best_load = load;
+        }
     }
-    p.part_per_group = (p.items_per_group + p.items_per_cta - 1) / p.items_per_cta + 1;
-    p.smem = attention_smem_bytes(G, d, p.items_per_cta * p.item_rows);
-    return p;
+    best.part_per_group = (best.items_per_group + best.items_per_cta - 1) / best.items_per_cta + 1;
+    best.smem = attention_smem_bytes(G, d, best.items_per_cta * best.item_rows);
+    return best;
 }
 
 size_t attention_part_floats(int G, int d, int B, int Hkv, int Nmax, int resident) {

@@ -34,7 +34,7 @@ constexpr int kMaxBatch = 256;
 constexpr size_t kMaxZsFloats = kMaxGroupRows * 8;    // logits, 8 per row      (4 MiB)
 // softmax partials: B*Hkv*part_per_group records of (16 + G*d) floats; this bound covers
 // B*Hkv*R <= 131,072 at the usual shapes, larger plans return TKV_ECAPACITY (checked per call)
-constexpr size_t kMaxPartFloats = (kMaxGroupRows / 128 + 2048 + 4096 + 64) * (16 + 8 * 128);   // ~29 MiB
+constexpr size_t kMaxPartFloats = (kMaxGroupRows / 64 + 2048 + 4096 + 64) * (16 + 8 * 128);    // ~34 MiB
 
 static __device__ __align__(256) float g_alpha_scratch[kMaxAlphaFloats];
 static __device__ __align__(256) float g_zs_scratch[kMaxZsFloats];

@@ -1010,7 +1010,9 @@ tkv_status tkv_decode_step(tkv_ctx* ctx, int32_t layer, const void* q, float* ou
     CK(cudaEventRecord(ctx->ev_attn[slotr], ctx->compute));
     if (ctx->capturing) {
         ctx->attn_in_capture[slotr] = true;
-        ctx->cap_rows = plan.items_per_group * plan.item_rows;
+        // the launch plan is a function of ceil(rmax / 64): replays stay within this 64-row bucket
+        // so that they run the geometry an eager step would
+        ctx->cap_rows = std::min(plan.items_per_group * plan.item_rows, (rmax + 63) / 64 * 64);
     }
     ctx->last_splits = plan.grid;
     ctx->decoded++;

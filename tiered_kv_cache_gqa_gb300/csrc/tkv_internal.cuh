@@ -21,8 +21,6 @@
 
 namespace tkv {
 
-constexpr int kRows = 32;               // rows per pipeline tile
-
 // Move kinds produced by a re-tier.
 enum MoveKind : int {
     MV_T0_T1 = 1,   // write back a T0 row to the host T1 store      (at re-tier)
@@ -103,7 +101,7 @@ struct AttnArgs {
     int32_t* err;                // status word (unused by kernels without device waits)
     int layer, L, B, Hq, Hkv, d, Nmax, S0, S1, S2;
     int items_per_group;         // ceil(max_b R_b / item_rows)
-    int item_rows;               // rows per item, a multiple of 128
+    int item_rows;               // rows per item: 64, 128 or 256
     int items_per_cta;           // contiguous items per CTA
     int grid;                    // CTAs of the main kernel
     int part_per_group;          // partial records per group (CTAs whose ranges can touch a group)
