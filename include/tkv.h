@@ -189,7 +189,7 @@ void tkv_destroy(tkv_ctx* ctx);
 /* Appends n_tokens new positions for one layer ("Four-tier classification":
  * new tokens fall in the recent window, so they enter T0).
  * k, v: device bf16 [B][n_tokens][Hkv][d].
- * k and v must be 16-byte aligned.
+ * k and v must be 16-byte aligned (TKV_EINVAL otherwise).
  * Protocol: a group of n tokens opens with layer 0 and every layer is
  * appended in order 0..L-1.  With n_tokens == 1 the group is a decode step:
  * tkv_decode_step(layer) follows tkv_append(layer), and the step closes after
@@ -313,7 +313,7 @@ tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* c
  * over a dense cache in which every position is retained and resident.
  *   q:   device bf16 [L][B][Hq][d]
  *   kv:  device bf16 [L][2][B][Hkv][R][d]   (K rows, then V rows; positions
- *        0..R-1 in logical order, the decoded token included)
+ *        0..R-1 in logical order, the decoded token included), 16-byte aligned
  *   out: device fp32 [L][B][Hq][d]
  *   s:   device fp32 [B][R], read and updated in place: s += the step's mean
  *        over layers and query heads of the attention weights
@@ -327,8 +327,8 @@ tkv_status tkv_profile_end(tkv_ctx* ctx, tkv_prof_entry* attn, tkv_prof_entry* c
  * and should come before any stream capture.  All calls share the scratch and
  * leave their contents in it, so calls that overlap on the GPU race.  The call
  * enqueues work and returns without waiting.
- * Errors: TKV_EINVAL (NULL pointers, shapes), TKV_ECAPACITY (beyond the
- * limits above), TKV_ECUDA. */
+ * Errors: TKV_EINVAL (NULL pointers, a misaligned kv, shapes), TKV_ECAPACITY
+ * (beyond the limits above), TKV_ECUDA. */
 tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, float* out, float* s,
                                     int32_t num_layers, int32_t batch, int32_t num_q_heads,
                                     int32_t num_kv_heads, int32_t head_dim, int32_t num_positions,

@@ -85,3 +85,12 @@ def test_host_link_probe_rejects_bad_sizes_without_a_gpu(lib_path):
     assert tkv.tkv_measure_host_link(0, 1000)[0] == tkv.TKV_EINVAL          # below 1 MiB
     assert tkv.tkv_measure_host_link(0, (1 << 20) + 8)[0] == tkv.TKV_EINVAL  # not a multiple of 16
     assert tkv.tkv_measure_host_link(-1, 1 << 20)[0] == tkv.TKV_EINVAL
+
+
+def test_noalloc_rejects_a_misaligned_cache_without_a_gpu(lib_path):
+    """kv rows are copied in 16-byte units: a misaligned kv is refused before any CUDA call
+    (the addresses are never dereferenced)."""
+    import tiered_kv_cache_gqa_gb300 as tkv
+    args = (1, 1, 8, 2, 128, 64)
+    assert tkv.tkv_decode_dense_noalloc(0x10000, 0x20008, 0x30000, 0x40000, *args, stream=0) == tkv.TKV_EINVAL
+    assert tkv.tkv_decode_dense_noalloc(0, 0x20000, 0x30000, 0x40000, *args, stream=0) == tkv.TKV_EINVAL

@@ -218,6 +218,9 @@ def test_call_order_and_capacity_errors_leave_context_usable():
     out = torch.empty(1, 4, 64, device="cuda")
     lib = tkv.load()
     assert tkv.tkv_append(ctx.ctx, 1, k, k, 1) == tkv.TKV_EINVAL          # layer 0 first
+    kflat = k.view(-1)
+    assert tkv.tkv_append(ctx.ctx, 0, kflat[1:].data_ptr(), k, 1) == tkv.TKV_EINVAL   # k not 16-byte aligned
+    assert tkv.tkv_append(ctx.ctx, 0, k, kflat[4:].data_ptr(), 1) == tkv.TKV_EINVAL   # v not 16-byte aligned
     assert tkv.tkv_append(ctx.ctx, 0, k, k, 11) == tkv.TKV_ECAPACITY       # beyond max_tokens
     assert tkv.tkv_decode_step(ctx.ctx, 0, q, out) == tkv.TKV_EINVAL       # nothing open
     assert tkv.tkv_retier(ctx.ctx) == tkv.TKV_OK

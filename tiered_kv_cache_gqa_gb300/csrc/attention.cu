@@ -74,7 +74,7 @@ struct AttnCfg {
     static constexpr int PS = 16 + G * D;            // floats of one (m[8], l[8], O[G][D]) record
     static constexpr size_t off_ring = 0;
     static constexpr size_t off_comb = kAttnWarps * sz_warp_ring;
-    static constexpr size_t off_n = off_comb + (size_t)kAttnWarps * PS * 4;   // rows of each item
+    static constexpr size_t off_n = off_comb + (size_t)PS * 4;   // rows of each item
     // per item: rows, decode-token flag, (sequence << 16 | KV head)
     static constexpr size_t off_mask = off_n + (size_t)(kMaxWindowRows / kMinItemRows) * 3 * 4;   // T2 rows per ring slot
     static constexpr size_t off_rl = off_mask + (size_t)kAttnWarps * kWarpStages * 4;
@@ -126,38 +126,45 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// Widens the T2 record at `row` (D E4M3 codes, then the fp32 scale) in place to a row of
-// D bf16 values (every E4M3 value is exact in bf16); returns the scale.
-template <int D>
-__device__ __forceinline__ float widen_t2_row(uint8_t* row) {
-    const float sc = *reinterpret_cast<const float*>(row + D);
-    uint4 codes[D / 16];
-#pragma unroll
-    for (int c = 0; c < D / 16; ++c) codes[c] = reinterpret_cast<const uint4*>(row)[c];
-#pragma unroll
-    for (int c = 0; c < D / 16; ++c) {
-        const uint32_t w[4] = {codes[c].x, codes[c].y, codes[c].z, codes[c].w};
-        uint32_t outw[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 lo = e4m3x2_to_float2((uint16_t)(w[i] & 0xFFFF));
-            const float2 hi = e4m3x2_to_float2((uint16_t)(w[i] >> 16));
+// Widens every T2 record of a ring stage (`mask`: its rows) in place to a row of D bf16
+// values (every E4M3 value is exact in bf16), the whole warp on one record at a time, D / 32
+// codes a lane; a record is D E4M3 codes followed by its fp32 scale.  `sc[i]` of the lanes
+// that hold tile row gq + 8 i in the product fragments is multiplied by that row's scale.
+template <int D, int ROWB, int NR>
+__device__ __forceinline__ void widen_t2_rows(uint8_t* stage, uint32_t mask, int lane, int gq, float (&sc)[NR]) {
+    while (mask != 0u) {
+        const int r = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        uint8_t* row = stage + (size_t)r * ROWB;
+        const float scale = *reinterpret_cast<const float*>(row + D);
+        if constexpr (D == 128) {
+            const uint32_t w = reinterpret_cast<const uint32_t*>(row)[lane];
+            const float2 lo = e4m3x2_to_float2((uint16_t)(w & 0xFFFFu));
+            const float2 hi = e4m3x2_to_float2((uint16_t)(w >> 16));
             const __nv_bfloat162 blo = __floats2bfloat162_rn(lo.x, lo.y);
             const __nv_bfloat162 bhi = __floats2bfloat162_rn(hi.x, hi.y);
-            outw[2 * i] = *reinterpret_cast<const uint32_t*>(&blo);
-            outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bhi);
+            __syncwarp();   // every lane has read its codes before any bf16 word lands on them
+            reinterpret_cast<uint2*>(row)[lane] =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&blo), *reinterpret_cast<const uint32_t*>(&bhi));
+        } else {
+            const uint16_t w = reinterpret_cast<const uint16_t*>(row)[lane];
+            const float2 f = e4m3x2_to_float2(w);
+            const __nv_bfloat162 bf = __floats2bfloat162_rn(f.x, f.y);
+            __syncwarp();
+            reinterpret_cast<uint32_t*>(row)[lane] = *reinterpret_cast<const uint32_t*>(&bf);
         }
-        reinterpret_cast<uint4*>(row)[2 * c] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-        reinterpret_cast<uint4*>(row)[2 * c + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+            if (r == gq + 8 * i) sc[i] *= scale;
     }
-    return sc;
+    __syncwarp();
 }
 
 // COMPACT: partly unrolled issue loops, for launches in which every warp streams one or
 // two tiles: the code then runs about once per launch and the instruction cache, not the
 // arithmetic, sets its pace.
 template <int G, int D, bool COMPACT>
-__global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
     constexpr int GP = C::GP, ROWB = C::ROWB, PS = C::PS;
     constexpr int kIssueUnroll = COMPACT ? 4 : 8;
@@ -310,13 +317,18 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
         }
     };
 
+    int consumed = 0;
+    // the copy of `consumed` has landed once at most kWarpStages - 1 later groups are pending
+    auto wait_slot = [&]() {
+        cp_async_commit();
+        cp_async_wait_prev();
+    };
     // the first kWarpStages - 1 copies (empty groups past the end of the sequence)
 #pragma unroll
     for (int i = 0; i < kWarpStages - 1; ++i) {
         issue_next();
         cp_async_commit();
     }
-    int consumed = 0;
 
     // ---------------------------------------------------- per-warp segment state
     // Tensor-core fragments (mma.m16n8k16, bf16 in, fp32 accumulate).  A lane holds, of a
@@ -351,59 +363,63 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     };
-    // merges the four warps' (m, l, O) of group g into this CTA's partial record for g
+    // merges the four warps' (m, l, O) of group g into this CTA's partial record for g: the
+    // warps fold their values into one shared record in warp order, then the CTA stores it
     auto flush_segment = [&](int g) {
-        float* cw = comb + (size_t)warp * PS;
         float l0 = l_r[0], l1 = l_r[1];
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
-        if (gq == 0) {
-            if (h0 < G) {
-                cw[h0] = m_r[0];
-                cw[8 + h0] = l0;
-            }
-            if (h1 < G) {
-                cw[h1] = m_r[1];
-                cw[8 + h1] = l1;
-            }
-        }
+        for (int w = 0; w < kAttnWarps; ++w) {
+            if (warp == w) {
+                // factors for the record so far (f_old) and this warp's values (f_new), per head
+                float f_old0 = 0.f, f_old1 = 0.f, f_new0 = 1.f, f_new1 = 1.f, M0 = m_r[0], M1 = m_r[1];
+                if (w > 0) {
+                    const float c0 = comb[h0 < G ? h0 : 0], c1 = comb[h1 < G ? h1 : 0];
+                    M0 = fmaxf(c0, m_r[0]);
+                    M1 = fmaxf(c1, m_r[1]);
+                    f_old0 = (c0 == -INFINITY) ? 0.f : exp2f(c0 - M0);
+                    f_old1 = (c1 == -INFINITY) ? 0.f : exp2f(c1 - M1);
+                    f_new0 = (m_r[0] == -INFINITY) ? 0.f : exp2f(m_r[0] - M0);
+                    f_new1 = (m_r[1] == -INFINITY) ? 0.f : exp2f(m_r[1] - M1);
+                }
 #pragma unroll
-        for (int dt = 0; dt < D / 16; ++dt) {
-            const int d = dt * 16 + gq;
-            if (h0 < G) {
-                cw[16 + h0 * D + d] = o[dt][0];
-                cw[16 + h0 * D + d + 8] = o[dt][2];
+                for (int dt = 0; dt < D / 16; ++dt) {
+                    const int d = dt * 16 + gq;
+                    float* c0p = comb + 16 + h0 * D + d;
+                    float* c1p = comb + 16 + h1 * D + d;
+                    if (h0 < G) {
+                        c0p[0] = w ? c0p[0] * f_old0 + o[dt][0] * f_new0 : o[dt][0];
+                        c0p[8] = w ? c0p[8] * f_old0 + o[dt][2] * f_new0 : o[dt][2];
+                    }
+                    if (h1 < G) {
+                        c1p[0] = w ? c1p[0] * f_old1 + o[dt][1] * f_new1 : o[dt][1];
+                        c1p[8] = w ? c1p[8] * f_old1 + o[dt][3] * f_new1 : o[dt][3];
+                    }
+                }
+                __syncwarp();
+                if (gq == 0) {
+                    if (h0 < G) {
+                        comb[8 + h0] = w ? comb[8 + h0] * f_old0 + l0 * f_new0 : l0;
+                        comb[h0] = M0;
+                    }
+                    if (h1 < G) {
+                        comb[8 + h1] = w ? comb[8 + h1] * f_old1 + l1 * f_new1 : l1;
+                        comb[h1] = M1;
+                    }
+                }
             }
-            if (h1 < G) {
-                cw[16 + h1 * D + d] = o[dt][1];
-                cw[16 + h1 * D + d + 8] = o[dt][3];
-            }
+            __syncthreads();
         }
-        __syncthreads();
         // record (g, this CTA's rank among the CTAs that touch g)
         const int c_lo = (g * IPG) / a.items_per_cta;
         float* pout = a.part + ((size_t)g * a.part_per_group + (blockIdx.x - c_lo)) * PS;
-        for (int i = tid; i < G * D + G; i += NT) {
-            const int h = i < G * D ? i / D : i - G * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, comb[w * PS + h]);
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) {
-                const float mw = comb[w * PS + h];
-                const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-                acc += f * (i < G * D ? comb[w * PS + 16 + i] : comb[w * PS + 8 + h]);
-            }
-            if (i < G * D) {
-                pout[16 + i] = acc;
-            } else {
-                pout[h] = M;
-                pout[8 + h] = acc;
-            }
+        for (int i = tid; i < G * D; i += NT) pout[16 + i] = comb[16 + i];
+        if (tid < G) {
+            pout[tid] = comb[tid];
+            pout[8 + tid] = comb[8 + tid];
         }
         __syncthreads();
     };
@@ -431,8 +447,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
 
             // ---------------------------------------------------------- K tile
             issue_next();                       // the V tile of this tile
-            cp_async_commit();
-            cp_async_wait_prev();
+            wait_slot();
             __syncwarp();
             const uint32_t tmask = mask_s[consumed % kWarpStages];
             // the decode token's rows go from the ring into their T0 slot (K now, V below)
@@ -453,14 +468,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
             float rs[2 * MT];
 #pragma unroll
             for (int i = 0; i < 2 * MT; ++i) rs[i] = a.qscale;
-            if (tmask != 0u) {
-                // every T2 record of the stage is widened in place to a bf16 row (E4M3 values are
-                // exact in bf16), row r by lane r; the scale of row r stays with lane r
-                const float my_sc = ((tmask >> lane) & 1u) ? widen_t2_row<D>(stage_k + (size_t)lane * ROWB) : 1.0f;
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < 2 * MT; ++i) rs[i] *= __shfl_sync(0xffffffffu, my_sc, gq + 8 * i);
-            }
+            // T2 records of the stage become bf16 rows in place; their scales join rs
+            if (tmask != 0u) widen_t2_rows<D, ROWB>(stage_k, tmask, lane, gq, rs);
             // two accumulator chains (even and odd 16-column steps of d), added at the end
             float s[MT][4], s2[MT][4];
 #pragma unroll
@@ -555,23 +564,23 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2) attn_kernel(const AttnArgs
 
             // ---------------------------------------------------------- V tile
             issue_next();                       // the next K tile
-            cp_async_commit();
-            cp_async_wait_prev();
+            wait_slot();
             __syncwarp();
             if (newr >= 0) store_new_row(1);
             {
                 uint8_t* stage_v = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
                 if (tmask != 0u) {
                     // T2 rows: widened in place as on the K side; p of such a row carries its scale
-                    const float my_sc = ((tmask >> lane) & 1u) ? widen_t2_row<D>(stage_v + (size_t)lane * ROWB) : 1.0f;
-                    __syncwarp();
+                    float vs[2 * MT];
+#pragma unroll
+                    for (int i = 0; i < 2 * MT; ++i) vs[i] = 1.0f;
+                    widen_t2_rows<D, ROWB>(stage_v, tmask, lane, gq, vs);
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
-                            const float vs = __shfl_sync(0xffffffffu, my_sc, mt * 16 + gq + 8 * hh);
-                            p[mt][2 * hh] *= vs;
-                            p[mt][2 * hh + 1] *= vs;
+                            p[mt][2 * hh] *= vs[2 * mt + hh];
+                            p[mt][2 * hh + 1] *= vs[2 * mt + hh];
                         }
                 }
                 const uint32_t vb = smem_u32(stage_v) + v_lane;

@@ -34,7 +34,7 @@ constexpr int kMaxBatch = 256;
 constexpr size_t kMaxZsFloats = kMaxGroupRows * 8;    // logits, 8 per row      (4 MiB)
 // softmax partials: B*Hkv*part_per_group records of (16 + G*d) floats; this bound covers
 // B*Hkv*R <= 131,072 at the usual shapes, larger plans return TKV_ECAPACITY (checked per call)
-constexpr size_t kMaxPartFloats = (kMaxGroupRows / 64 + 2048 + 4096 + 64) * (16 + 8 * 128);    // ~34 MiB
+constexpr size_t kMaxPartFloats = (kMaxGroupRows / 128 + 2048 + 4096 + 64) * (16 + 8 * 128);   // ~29 MiB
 
 static __device__ __align__(256) float g_alpha_scratch[kMaxAlphaFloats];
 static __device__ __align__(256) float g_zs_scratch[kMaxZsFloats];
@@ -94,6 +94,7 @@ extern "C" tkv_status tkv_decode_dense_noalloc(const void* q, const void* kv, fl
     const int L = num_layers, B = batch, Hq = num_q_heads, Hkv = num_kv_heads, d = head_dim;
     const int R = num_positions;
     if (!q || !kv || !out || !s) return TKV_EINVAL;
+    if (reinterpret_cast<uintptr_t>(kv) & 15u) return TKV_EINVAL;   // rows are copied in 16-byte units
     if (L < 1 || B < 1 || Hkv < 1 || Hq < 1 || R < 1 || Hq % Hkv || Hq / Hkv > 8 || (d != 64 && d != 128))
         return TKV_EINVAL;
     // size limits of the fixed scratch

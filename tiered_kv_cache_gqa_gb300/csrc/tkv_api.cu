@@ -886,6 +886,8 @@ void tkv_destroy(tkv_ctx* ctx) {
 tkv_status tkv_append(tkv_ctx* ctx, int32_t layer, const void* k, const void* v, int32_t n_tokens) {
     CHECK_CTX();
     if (!k || !v || n_tokens < 1 || layer < 0 || layer >= ctx->L) return TKV_EINVAL;
+    // rows are copied in 16-byte units
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) return TKV_EINVAL;
     if (n_tokens > 1 && ctx->capturing) return TKV_EINVAL;
     DeviceGuard guard(ctx->device);
     if (n_tokens > 1) drop_graph(ctx);
