@@ -11,16 +11,17 @@
 // Work split.  The retained list of every (sequence b, KV head) group is cut
 // into items of `item_rows` consecutive positions.  The main kernel runs
 // persistent CTAs of four warps; CTA c owns a contiguous range of items in
-// (b, KV head, item) order.  Within an item, warp w owns the 32-row tiles w and
-// w + 4.  Each warp streams, item after item, the K rows and then the V rows
-// of its tiles through its own two-stage shared-memory ring with 16-byte
+// (b, KV head, item) order.  Within an item, warp w owns the tiles w, w + 4,
+// ... of 16 rows (32 in the compact instantiation).  Each warp streams, item
+// after item, the K rows and then the V rows of its tiles through its own
+// shared-memory ring (4 slots of 16-row tiles, or 2 of 32) with 16-byte
 // cp.async (16 lanes per 256-byte row, every row fetched from its home: T0
 // pool, T1 staging or T2 records; the group's decode token from the caller's
-// k/v, stored into its T0 slot from the ring), so the next tile -- possibly
-// of the next item -- is in flight while the current one is computed.  The
+// k/v, stored into its T0 slot from the ring), so the next tiles -- possibly
+// of the next item -- are in flight while the current one is computed.  The
 // only waits are cp.async.wait_group and CTA barriers; there are no spin loops.
 //   K tile:  tensor cores (mma.m16n8k16, bf16 operands, fp32 accumulators):
-//            S^T = K q^T for the tile's 32 rows and the group's query heads,
+//            S^T = K q^T for the tile's rows and the group's query heads,
 //            K from the ring by ldmatrix, q^T in registers; z = S^T *
 //            log2(e)/sqrt(d) (times the record's scale for a T2 row, whose
 //            E4M3 codes are first widened in place to bf16, exactly).
@@ -51,8 +52,10 @@
 namespace tkv {
 
 constexpr int kAttnWarps = 4;
-constexpr int kTileRows = 16;             // rows per pipeline tile (one m16 block of the products)
-constexpr int kWarpStages = 4;            // tiles per warp ring: three in flight while one is used
+constexpr int kRingRows = 64;             // rows of a warp's ring: 4 slots of 16-row tiles (three in
+                                          // flight while one is used), or, in the compact instantiation,
+                                          // 2 slots of 32-row tiles (fewer serial steps per warp)
+constexpr int kMaxSlots = 4;
 constexpr int kCompactRows = 256;         // CTA windows up to this many rows use the compact instantiation
 constexpr int kMinItemRows = 128;         // item sizes: 128 or 256 rows
 constexpr int kMaxWindowRows = 3584;       // retained-list rows a CTA stages in shared memory
@@ -69,15 +72,14 @@ struct AttnCfg {
     static_assert(D == 64 || D == 128, "head_dim must be 64 or 128");
     static_assert(G >= 1 && G <= 8, "group size must be 1..8");
 
-    static constexpr size_t sz_stage = (size_t)kTileRows * ROWB;
-    static constexpr size_t sz_warp_ring = kWarpStages * sz_stage;
+    static constexpr size_t sz_warp_ring = (size_t)kRingRows * ROWB;
     static constexpr int PS = 16 + G * D;            // floats of one (m[8], l[8], O[G][D]) record
     static constexpr size_t off_ring = 0;
     static constexpr size_t off_comb = kAttnWarps * sz_warp_ring;
     static constexpr size_t off_n = off_comb + (size_t)PS * 4;   // rows of each item
     // per item: rows, decode-token flag, (sequence << 16 | KV head)
     static constexpr size_t off_mask = off_n + (size_t)(kMaxWindowRows / kMinItemRows) * 3 * 4;   // T2 rows per ring slot
-    static constexpr size_t off_rl = off_mask + (size_t)kAttnWarps * kWarpStages * 4;
+    static constexpr size_t off_rl = off_mask + (size_t)kAttnWarps * kMaxSlots * 4;
 
     static size_t smem(int rl_rows) { return off_rl + (size_t)rl_rows * 4; }
 };
@@ -86,8 +88,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_prev() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(kWarpStages - 1) : "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // 4 bytes global -> shared
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
@@ -160,14 +163,17 @@ __device__ __forceinline__ void widen_t2_rows(uint8_t* stage, uint32_t mask, int
     __syncwarp();
 }
 
-// COMPACT: partly unrolled issue loops, for launches in which every warp streams one or
-// two tiles: the code then runs about once per launch and the instruction cache, not the
+// COMPACT: 32-row tiles in two ring slots and partly unrolled issue loops, for launches in
+// which a CTA streams at most 256 rows: the code then runs about once per launch and the instruction cache, not the
 // arithmetic, sets its pace.
 template <int G, int D, bool COMPACT>
 __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
     constexpr int GP = C::GP, ROWB = C::ROWB, PS = C::PS;
     constexpr int kIssueUnroll = COMPACT ? 4 : 8;
+    constexpr int kTileRows = COMPACT ? 32 : 16;        // rows per pipeline tile
+    constexpr int kWarpStages = kRingRows / kTileRows;  // ring slots
+    constexpr size_t kStageBytes = (size_t)kTileRows * ROWB;
     constexpr int MT = kTileRows / 16;                  // 16-row blocks of a tile
     constexpr int NT = kAttnWarps * 32;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -277,7 +283,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
             src = row_v;
         }
         if (kv == 0) all_bf16_issue = __all_sync(0xffffffffu, lane >= kTileRows || row_bytes == 2 * D);
-        const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * C::sz_stage);
+        const uint32_t dst0 = smem_u32(ring + (size_t)(issued % kWarpStages) * kStageBytes);
         const int col = lane & 15, half = lane >> 4;
         if (all_bf16_issue) {
             // kTileRows bf16 rows: no per-row kinds to decode
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
     // the copy of `consumed` has landed once at most kWarpStages - 1 later groups are pending
     auto wait_slot = [&]() {
         cp_async_commit();
-        cp_async_wait_prev();
+        cp_async_wait_group<kWarpStages - 1>();
     };
     // the first kWarpStages - 1 copies (empty groups past the end of the sequence)
 #pragma unroll
@@ -455,14 +461,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
             auto store_new_row = [&](int kv) {
                 if (lane < 2 * D / 16) {
                     const int slot = loc_slot(rl_s[(size_t)(item - it0) * IT + tile * kTileRows + newr]);
-                    const uint8_t* srow = ring + (size_t)(consumed % kWarpStages) * C::sz_stage + (size_t)newr * ROWB;
+                    const uint8_t* srow = ring + (size_t)(consumed % kWarpStages) * kStageBytes + (size_t)newr * ROWB;
                     uint8_t* drow = reinterpret_cast<uint8_t*>(const_cast<__nv_bfloat16*>(a.k0v0)) +
                                     row_index(a.layer, kv, b, kvh, slot, a.B, a.Hkv, a.S0) * (2 * D);
                     reinterpret_cast<uint4*>(drow)[lane] = reinterpret_cast<const uint4*>(srow)[lane];
                 }
             };
             if (newr >= 0) store_new_row(0);
-            uint8_t* stage_k = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
+            uint8_t* stage_k = ring + (size_t)(consumed % kWarpStages) * kStageBytes;
             // row scales of this lane's score rows (tile rows gq + 8 i): log2(e)/sqrt(d), times
             // the record's scale for a T2 row
             float rs[2 * MT];
@@ -568,7 +574,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
             __syncwarp();
             if (newr >= 0) store_new_row(1);
             {
-                uint8_t* stage_v = ring + (size_t)(consumed % kWarpStages) * C::sz_stage;
+                uint8_t* stage_v = ring + (size_t)(consumed % kWarpStages) * kStageBytes;
                 if (tmask != 0u) {
                     // T2 rows: widened in place as on the K side; p of such a row carries its scale
                     float vs[2 * MT];
