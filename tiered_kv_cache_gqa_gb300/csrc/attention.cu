@@ -369,14 +369,68 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     };
-    // merges the four warps' (m, l, O) of group g into this CTA's partial record for g: the
-    // warps fold their values into one shared record in warp order, then the CTA stores it
-    auto flush_segment = [&](int g) {
+    // merges the four warps' (m, l, O) of group g into this CTA's partial record for g and
+    // stores it at (g, this CTA's rank among the CTAs that touch g).  At the end of the CTA's
+    // run (`last`) every copy has been consumed, so each warp parks its record in its own idle
+    // ring and the four records merge in one pass (fixed warp order); earlier, while later
+    // tiles may be in flight in the rings, the warps fold their values into one shared record
+    // in warp order.
+    auto flush_segment = [&](int g, bool last) {
         float l0 = l_r[0], l1 = l_r[1];
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        const int c_lo = (g * IPG) / a.items_per_cta;
+        float* pout = a.part + ((size_t)g * a.part_per_group + (blockIdx.x - c_lo)) * PS;
+        if (last) {
+            float* cw = reinterpret_cast<float*>(ring);
+            if (gq == 0) {
+                if (h0 < G) {
+                    cw[h0] = m_r[0];
+                    cw[8 + h0] = l0;
+                }
+                if (h1 < G) {
+                    cw[h1] = m_r[1];
+                    cw[8 + h1] = l1;
+                }
+            }
+#pragma unroll
+            for (int dt = 0; dt < D / 16; ++dt) {
+                const int d = dt * 16 + gq;
+                if (h0 < G) {
+                    cw[16 + h0 * D + d] = o[dt][0];
+                    cw[16 + h0 * D + d + 8] = o[dt][2];
+                }
+                if (h1 < G) {
+                    cw[16 + h1 * D + d] = o[dt][1];
+                    cw[16 + h1 * D + d + 8] = o[dt][3];
+                }
+            }
+            __syncthreads();
+            const float* rec0 = reinterpret_cast<const float*>(smem + C::off_ring);
+            constexpr size_t kRecStride = C::sz_warp_ring / sizeof(float);
+            for (int i = tid; i < G * D + G; i += NT) {
+                const int h = i < G * D ? i / D : i - G * D;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, rec0[w * kRecStride + h]);
+                float acc = 0.f;
+#pragma unroll
+                for (int w = 0; w < kAttnWarps; ++w) {
+                    const float mw = rec0[w * kRecStride + h];
+                    const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                    acc += f * (i < G * D ? rec0[w * kRecStride + 16 + i] : rec0[w * kRecStride + 8 + h]);
+                }
+                if (i < G * D) {
+                    pout[16 + i] = acc;
+                } else {
+                    pout[h] = M;
+                    pout[8 + h] = acc;
+                }
+            }
+            return;
         }
         for (int w = 0; w < kAttnWarps; ++w) {
             if (warp == w) {
@@ -419,9 +473,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
             }
             __syncthreads();
         }
-        // record (g, this CTA's rank among the CTAs that touch g)
-        const int c_lo = (g * IPG) / a.items_per_cta;
-        float* pout = a.part + ((size_t)g * a.part_per_group + (blockIdx.x - c_lo)) * PS;
         for (int i = tid; i < G * D; i += NT) pout[16 + i] = comb[16 + i];
         if (tid < G) {
             pout[tid] = comb[tid];
@@ -440,7 +491,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
         const int j0 = (item % IPG) * IT;
         const int n = n_s[item - it0];
         if (g != cur_group) {
-            if (cur_group >= 0) flush_segment(cur_group);
+            if (cur_group >= 0) flush_segment(cur_group, false);
             load_q(g);
             reset_segment();
             cur_group = g;
@@ -618,7 +669,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
             ++consumed;
         }
     }
-    flush_segment(cur_group);
+    flush_segment(cur_group, true);
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
@@ -627,12 +678,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
 // heads of alpha = 2^(z - M) / L.  Every load of the block is issued before the
 // first barrier (the segment statistics, the block's share of the partial
 // outputs, the logits of its rows), so the kernel costs about one memory round
-// trip after the main kernel ends.
-template <int G, int D>
-__global__ void __launch_bounds__(256, 1) attn_combine_kernel(const AttnArgs a) {
+// trip after the main kernel ends.  SEG partial outputs are loaded per thread before
+// the barrier: 32 for launches whose groups have many partials (small batches, where
+// latency rules), 8 otherwise (fewer registers: four blocks per SM instead of two).
+template <int G, int D, int SEG>
+__global__ void __launch_bounds__(256, SEG <= 8 ? 4 : 1) attn_combine_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
     constexpr int GP = C::GP, PS = C::PS;
-    constexpr int kSegBatch = 32;                    // partial outputs loaded per thread at once
+    constexpr int kSegBatch = SEG;                   // partial outputs loaded per thread at once
     extern __shared__ __align__(16) float fsm[];     // m[seg][8], l[seg][8], then f[seg][8]
     __shared__ float Ms[8], Linv[8];
     // launched as a programmatic dependent of the main kernel: wait for its results
@@ -764,13 +817,13 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st, cudaEvent_t aft
     cfg.gridDim = dim3(blocks, a.B * a.Hkv);
     cfg.blockDim = dim3(kCombineThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)max_segs * 3 * 8 * 4;
+    auto kernel = max_segs <= 8 ? attn_combine_kernel<G, D, 8> : attn_combine_kernel<G, D, 32>;
     if (cfg.dynamicSmemBytes > 48 * 1024) {
         // raise the limit if needed, never lower it (other contexts may need more)
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, attn_combine_kernel<G, D>);
+        e = cudaFuncGetAttributes(&fa, kernel);
         if (e == cudaSuccess && (size_t)fa.maxDynamicSharedSizeBytes < cfg.dynamicSmemBytes)
-            e = cudaFuncSetAttribute(attn_combine_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)cfg.dynamicSmemBytes);
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return e;
     }
     cfg.stream = st;
@@ -779,7 +832,7 @@ static cudaError_t launch_gd(const AttnArgs& a, cudaStream_t st, cudaEvent_t aft
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_combine_kernel<G, D>, a);
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 template <int G, int D>
@@ -790,7 +843,10 @@ static cudaError_t prepare_gd(size_t smem) {
     if (e != cudaSuccess) return e;
     // the combine kernel asks for the same shared-memory carve-out as the main kernel, so that
     // an SM need not be reconfigured between the two
-    return cudaFuncSetAttribute(attn_combine_kernel<G, D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(attn_combine_kernel<G, D, 8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(attn_combine_kernel<G, D, 32>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 (int)cudaSharedmemCarveoutMaxShared);
 }
 
