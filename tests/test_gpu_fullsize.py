@@ -1,5 +1,6 @@
 """Parity at full per-launch sizes, in the launch configurations the bench
-times: the 7B-shaped stack (28 layers, batch 1, 28/4 heads, 2,512 positions;
+times: a head_dim-64 stack with an odd group (2 layers, batch 8, 24/8 heads,
+6,000 positions), the 7B-shaped stack (28 layers, batch 1, 28/4 heads, 2,512 positions;
 the compact instantiation), the 14B-shaped stack (48 layers, batch 8, 40/8
 heads, 4,096 positions), 32B-shaped layers (batch 4, 8,192 positions, x20
 outlier channels; 8 of its 64 layers) and 70B-shaped layers (batch 8, 64/8
@@ -24,9 +25,15 @@ from harness import ATOL_OUT, gpu_step
 
 pytestmark = pytest.mark.gpu
 
+# head_dim 64 and an odd group (G = 3: heads past G are zero columns of the products) at a size
+# that runs the persistent instantiation with several items per CTA
+D64 = synth.Workload("d64", 2, 24, 8, 64, 8, prompt_len=256, prefill_len=6000, decode_steps=1,
+                     window=64, outlier_rate=0.001)
+
 CASES = {
     # name: (workload, pre-filled positions (the decoded token adds one), layers, samples,
     #        fewest CTAs the attention launch must use: two per SM for the large ones)
+    "d64_g3": (D64, 5999, None, [(0, 0, 0), (1, 7, 7), (1, 3, 2), (0, 5, 4)], 304),
     "7b": ("7b", 2511, None, [(0, 0, 0), (27, 0, 3), (13, 0, 2)], 40),
     "14b": ("14b", 4095, None, [(0, 0, 0), (47, 7, 7), (23, 3, 5), (11, 5, 2), (36, 1, 4)], 304),
     "32b": ("32b", 8191, 8, [(0, 0, 0), (7, 3, 7), (4, 2, 5)], 304),
@@ -85,7 +92,8 @@ def oracle_group(WL, N, gen, tiers, q, k, v, layer, b, kvh):
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_full_size_sampled_parity_and_proposition_1(case):
     name, N, layers, samples, min_ctas = CASES[case]
-    WL = synth.WORKLOADS[name].with_(prefill_len=N, decode_steps=1, ratios=(0.3, 0.5, 0.15, 0.05), seed=77)
+    base = synth.WORKLOADS[name] if isinstance(name, str) else name
+    WL = base.with_(prefill_len=N, decode_steps=1, ratios=(0.3, 0.5, 0.15, 0.05), seed=77)
     if layers:
         WL = WL.with_(num_layers=layers)
     gen = synth.Generator(WL, device="cuda")
