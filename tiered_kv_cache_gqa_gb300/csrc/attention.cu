@@ -42,8 +42,9 @@
 // boundaries, the CTA ranges and every reduction order depend only on the
 // retained counts, never on which tier a row sits in, so a row read from T0 or
 // from T1 staging gives bit-identical results.  No atomics touch `out` or `g`.
-// Launches in which every warp streams at most two tiles use a compact
-// instantiation (partly unrolled issue loops, same arithmetic in the same order).
+// Launches in which a CTA streams at most 256 rows use a compact instantiation
+// (32-row tiles in two ring slots, partly unrolled issue loops); the launch plan,
+// and with it the instantiation, depends on the retained counts only.
 #include <algorithm>
 #include <cmath>
 
@@ -164,8 +165,9 @@ __device__ __forceinline__ void widen_t2_rows(uint8_t* stage, uint32_t mask, int
 }
 
 // COMPACT: 32-row tiles in two ring slots and partly unrolled issue loops, for launches in
-// which a CTA streams at most 256 rows: the code then runs about once per launch and the instruction cache, not the
-// arithmetic, sets its pace.
+// which a CTA streams at most 256 rows: there every warp runs one or two tiles, so fewer serial
+// steps per warp pay, and the code runs about once per launch, so the instruction cache, not
+// the arithmetic, sets its pace.
 template <int G, int D, bool COMPACT>
 __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs a) {
     using C = AttnCfg<G, D>;
@@ -503,7 +505,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
             const int nrows = min(kTileRows, n - tile * kTileRows);
 
             // ---------------------------------------------------------- K tile
-            issue_next();                       // the V tile of this tile
+            issue_next();                       // the copy kWarpStages - 1 ahead in this warp's sequence
             wait_slot();
             __syncwarp();
             const uint32_t tmask = mask_s[consumed % kWarpStages];
@@ -620,7 +622,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 3) attn_kernel(const AttnArgs
             }
 
             // ---------------------------------------------------------- V tile
-            issue_next();                       // the next K tile
+            issue_next();                       // and the one after it
             wait_slot();
             __syncwarp();
             if (newr >= 0) store_new_row(1);
