@@ -616,6 +616,13 @@ def hbm_projection(wl, args):
     return f.saved_bytes
 
 
+def link_bound_step_ms(t1_bytes_per_step, link):
+    """Time a step's T1 rows take at the measured copy-engine link peak (ms), or None."""
+    if not link or not link.get("h2d_ce_gbs") or t1_bytes_per_step <= 0:
+        return None
+    return t1_bytes_per_step / (link["h2d_ce_gbs"] * 1e9) * 1e3
+
+
 def link_fraction(gbs, link):
     """A host-link rate as fractions of the measured link peak and of nominal PCIe Gen5 x16."""
     if gbs is None:
@@ -686,6 +693,7 @@ def main():
     delta_gbs = pd["bytes"] / (pd["ms"] / 1e3) / 1e9 if pd["ms"] > 0 else None
     link_ms = p1["ms"] + pd["ms"]
     tl = timeline(args.steps, args.warmup, wl.delta)
+    link_floor = link_bound_step_ms(p1["bytes"] / KP_ if KP_ else 0.0, r["link"])
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -732,6 +740,11 @@ def main():
             "kv_full_cache_bytes": st["kv_bytes_full_cache"],
             "tier_count": st["tier_count"],
             "step_ms_median": statistics.median(tm["step_ms"]),
+            "host_link_floor": link_floor and {
+                "ms_per_step": link_floor,
+                "timed_steps_within_10pct": sum(1 for x in tm["step_ms"] if x <= 1.1 * link_floor),
+                "note": "a step's T1 bytes at the link peak measured in this run: no step can be faster "
+                        "while T1 crosses the link every step; slower steps read the host store slower"},
         },
     }
     print(json.dumps(line))

@@ -95,3 +95,12 @@ def test_both_arms_describe_the_same_config():
     ref = bench.parse(["--impl", "reference", "--workload", "70b", "--steps", "20", "--warmup", "5"])
     assert bench.run_config(args, wl) == bench.run_config(ref, bench.bench_workload("70b", 5, 20))
     assert bench.run_config(args, wl)["retier_steps_timed"] == [192]
+
+
+def test_host_link_floor_of_a_step():
+    """The link-bound step time: a step's T1 bytes at the measured copy-engine peak."""
+    import bench
+    assert abs(bench.link_bound_step_ms(211.5e9 * 0.138, {"h2d_ce_gbs": 211.5}) - 138.0) < 1e-9
+    assert bench.link_bound_step_ms(0.0, {"h2d_ce_gbs": 211.5}) is None
+    assert bench.link_bound_step_ms(1e9, None) is None
+    assert bench.link_bound_step_ms(1e9, {"h2d_ce_gbs": 0.0}) is None
