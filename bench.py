@@ -148,7 +148,7 @@ def run_config(args, wl):
     """The `config` object of the JSON line; identical in both arms for the same arguments."""
     graph = args.mode == "graph" and args.t1 != "split"
     tl = timeline(args.steps, args.warmup, wl.delta)
-    return {"workload": describe(wl), "inputs": "bf16 K/V/q (T2 rows FP8-E4M3), fp32 arithmetic",
+    return {"workload": describe(wl), "inputs": "bf16 K/V/q (T2 rows FP8-E4M3)",
             "global_batch": wl.batch * args.gpus, "seq_len": TARGET_N[args.workload],
             "parallelism": "replicas (sequence shards)", "t1_transport": args.t1,
             "t2_placement": args.t2, "steps_as": "graph" if graph else "eager",
@@ -697,7 +697,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": run_config(args, wl),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
